@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode attention layer-step on GB300.
+
+One step = one decode layer-step of the whole batch: reshape_and_cache of the
+new token of every sequence, then decode attention through the block tables
+(split kernel + log-sum-exp merge, or the single pass).  Inputs are seeded
+synthetic workloads resident in HBM; L2 is flushed (a 256 MiB write) before
+every step and only the step's own kernels sit between its CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama8b]
+    python bench.py --impl reference ...   # the CPU reference on host cores
+
+Prints one JSON line (rank 0).  Metric: KV GB/s of the layer-step, with
+bytes = K/V of every context token read + q read + output written.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_226_gb300 import build as pa_build  # noqa: E402
+from paged_kv_cache_226_gb300 import inputs as pin  # noqa: E402
+from paged_kv_cache_226_gb300 import lib  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; µs per layer-step"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+DECODE_KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_226_gb300", "csrc", "decode_kernel.cuh")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(path=DECODE_KERNEL_SRC) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(config: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        p = json.load(f)
+    if p.get("source_sha256_16") != source_hash():
+        return None
+    return p.get("dram_bytes_per_launch")
+
+
+def step_bytes(w: pin.Workload, mode: str, partition: int):
+    """Algorithmic bytes: the layer-step and each kernel of it."""
+    e = 2
+    B, hq, hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+    kv = w.kv_bytes_logical()
+    q = B * hq * d * e
+    out = B * hq * d * e
+    new_tok = w.num_tokens * hkv * d * e * 2           # read k, v
+    write_tok = int((w.slot_mapping >= 0).sum()) * hkv * d * e * 2
+    parts = sum(-(-int(L) // partition) for L in w.context_lens)
+    split_w = parts * hq * (d + 2) * 4                  # tmp_out + max_logits + exp_sums
+    kernels = {"reshape_and_cache": new_tok + write_tok + w.num_tokens * 8}
+    if mode == "split":
+        kernels["paged_decode_split"] = kv + q + split_w
+        kernels["lse_reduce"] = split_w + out
+    else:
+        kernels["paged_decode"] = kv + q + out
+    return {"layer_step": kv + q + out, "kernels": kernels, "partitions": parts}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.strip().split(", ") for r in self.f.read().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_step(d, w, mode, partition, S, ws, out, evs=None, stream=None):
+    if evs:
+        evs[0].record(stream)
+    lib.reshape_and_cache(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"], d["v_cache"])
+    if evs:
+        evs[1].record(stream)
+    if mode == "split":
+        tmp, ml, es = ws
+        lib.decode_split(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                         d["context_lens"], w.scale, partition, S, tmp, ml, es)
+        if evs:
+            evs[2].record(stream)
+        lib.reduce(tmp, ml, es, d["context_lens"], partition, d["k_cache"],
+                   w.max_blocks_per_seq, out)
+    else:
+        lib.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                   w.scale, out)
+        if evs:
+            evs[2].record(stream)
+    if evs:
+        evs[3].record(stream)
+
+
+def cpu_baseline(w: pin.Workload, budget_s: float = 12.0):
+    """The CPU reference as it stands, timed on the host cores over whole
+    passes of the workload (at least one, up to ~budget_s)."""
+    import oracle
+    qb, kc, vc = pin.bits(w.q), pin.bits(w.k_cache), pin.bits(w.v_cache)
+    kn, vn = pin.bits(w.k_new), pin.bits(w.v_new)
+    bytes_per = w.kv_bytes_logical() + w.qo_bytes()
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        kc2, vc2, _ = oracle.reshape_and_cache(kn, vn, w.slot_mapping, kc, vc, w.block_size)
+        oracle.paged_decode(qb, kc2, vc2, w.block_tables, w.context_lens, w.scale, w.dtype)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el / passes * (passes + 1) > 2.5 * budget_s:
+            break
+    return {"value": passes * bytes_per / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{passes} full pass(es) of the {w.name} workload (reshape_and_cache + fp64 "
+                      f"paged decode of all {w.num_seqs} sequences), {el:.1f} s"}
+
+
+def bench_reference(args):
+    """CPU reference on the host cores; each step one full pass of the workload
+    (or of its first sequences when a pass would take longer than ~3 s)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = pin.build_workload(args.config)
+    qb, kc, vc = pin.bits(w.q), pin.bits(w.k_cache), pin.bits(w.v_cache)
+    kn, vn = pin.bits(w.k_new), pin.bits(w.v_new)
+    # size the per-step sample: whole sequences, about 3 s of work at most
+    t0 = time.perf_counter()
+    oracle.paged_decode(qb[:1], kc, vc, w.block_tables[:1], w.context_lens[:1], w.scale, w.dtype)
+    per_tok = (time.perf_counter() - t0) / max(1, int(w.context_lens[0]))
+    n = w.num_seqs
+    while n > 1 and per_tok * int(w.context_lens[:n].sum()) / max(1, oracle.max_threads()) > 3.0:
+        n = max(1, n // 2)
+    sl = slice(0, n)
+
+    def step():
+        kc2, vc2, _ = oracle.reshape_and_cache(kn[sl], vn[sl], w.slot_mapping[sl], kc, vc,
+                                               w.block_size)
+        oracle.paged_decode(qb[sl], kc2, vc2, w.block_tables[sl], w.context_lens[sl], w.scale,
+                            w.dtype)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    e = 2
+    bytes_step = int(w.context_lens[sl].astype(np.int64).sum()) * w.num_kv_heads * \
+        w.head_dim * e * 2 + 2 * n * w.num_q_heads * w.head_dim * e
+    value = bytes_step * args.steps / el / 1e9
+    sample = (f"first {n} of {w.num_seqs} sequences of the {w.name} workload per step "
+              f"(reshape_and_cache + fp64 paged decode)")
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": f"{w.name}: {pin.DESCRIPTIONS[w.name]}",
+                       "l2": "n/a (host)", "mode": "cpu oracle"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                             "cores": oracle.max_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args):
+    rank, world, local_rank = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pa_build.build()
+    lib.load()
+
+    seed = pin.CONFIGS[args.config][0] + 1000 * rank
+    w = pin.build_workload(args.config, seed=seed)
+    max_len = int(w.context_lens.max())
+    mode = args.mode if args.mode != "auto" else lib.choose_mode(
+        w.num_seqs, w.num_kv_heads, max_len, args.partition)
+    partition = args.partition
+    S = lib.num_partitions(max_len, partition)
+
+    d = {k: v.to(dev) for k, v in dict(
+        q=w.q, k_new=w.k_new, v_new=w.v_new, k_cache=w.k_cache, v_cache=w.v_cache,
+        block_tables=torch.from_numpy(w.block_tables),
+        context_lens=torch.from_numpy(w.context_lens),
+        slot_mapping=torch.from_numpy(w.slot_mapping)).items()}
+    ws = lib.split_workspace(d["q"], S) if mode == "split" else None
+    out = torch.empty_like(d["q"])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nb = step_bytes(w, mode, partition)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        run_step(d, w, mode, partition, S, ws, out)
+    torch.cuda.synchronize(dev)
+    assert lib.read_device_errors(dev) == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        time.sleep(0.3)
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            run_step(d, w, mode, partition, S, ws, out, evs[i], stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    k3_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    errs = lib.read_device_errors(dev)
+
+    # end to end through the public API: pinned host inputs -> device, the
+    # layer-step, output -> host, every step
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (torch.from_numpy(getattr(w, k)) if isinstance(getattr(w, k), np.ndarray)
+                    else getattr(w, k)).pin_memory()
+                for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+        for it in range(args.warmup + args.steps):
+            if it == args.warmup:
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+            flush.fill_(0.5)
+            for k, t in host.items():
+                d[k].copy_(t, non_blocking=True)
+            lib.reshape_and_cache(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
+                                  d["v_cache"])
+            lib.paged_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                d["context_lens"], w.scale, max_len, out=out, mode=mode,
+                                partition_size=partition, workspace=ws)
+            out_h.copy_(out, non_blocking=True)
+            stream.synchronize()
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        e2e = {"value": round(nb["layer_step"] * world / e2e_s / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s * 1e3, 4),
+               "note": "includes a 256 MiB L2-flush write per step"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm, peak_src = peaks()
+    dom = "paged_decode_split" if mode == "split" else "paged_decode"
+    dom_ms = sum(k2_ms) / len(k2_ms)
+    dom_bytes = nb["kernels"][dom]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    value = nb["layer_step"] * world / (ms * 1e-3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "us_per_layer_step": round(ms * 1e3, 2),
+        "hbm_frac_of_measured" if peak_src == "measured" else "hbm_frac_of_fallback":
+            round(value / world / hbm, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
+        "config": {"workload": f"{w.name}: {pin.DESCRIPTIONS[w.name]}", "mode": mode,
+                   "partition_tokens": partition if mode == "split" else None,
+                   "l2": "flushed before every step (256 MiB write, outside the step's events)",
+                   "kv_bytes": w.kv_bytes_logical(), "kv_bytes_unique": w.kv_bytes_unique(),
+                   "bytes_per_step": nb["layer_step"], "seqs_per_gpu": w.num_seqs},
+        "kernels_us": {"reshape_and_cache": round(1e3 * sum(k1_ms) / len(k1_ms), 2),
+                       dom: round(1e3 * dom_ms, 2)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2),
+                     "peak": hbm, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "traffic": profiled_traffic(args.config, dom)},
+        "clocks": clk.summary(),
+        "gpu_launches": 3 * args.steps if mode == "split" else 2 * args.steps,
+        "device_errors": errs,
+        "wall_s_timed": round(t_wall, 4),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if mode == "split":
+        line["kernels_us"]["lse_reduce"] = round(1e3 * sum(k3_ms) / len(k3_ms), 2)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama8b", choices=sorted(pin.CONFIGS))
+    ap.add_argument("--mode", default="auto", choices=["auto", "single", "split"])
+    ap.add_argument("--partition", type=int, default=lib.DEFAULT_PARTITION)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)        # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,176 @@
+/*
+ * pa.h -- C ABI of the paged decode attention library (libpa.so).
+ *
+ * The operation (from the pages on vLLM / PagedAttention):
+ *   - The KV cache is split into fixed-size blocks (16 tokens by default) that
+ *     may sit anywhere in a preallocated physical pool; a per-request block
+ *     table maps logical block j to its physical block (techfeed summary of
+ *     ngrok's "Serving models at scale with vLLM", section on PagedAttention;
+ *     youngju.dev "vLLM inference optimization", section "PagedAttention").
+ *   - A new token's K and V go to slot (last block, count % block_size)
+ *     (youngju.dev post, PagedAttentionManager.append_token).
+ *   - Decode attention follows the table, gathering K and V while it computes
+ *     (ta-paperlens "LLM serving from scratch", section on fragmentation and
+ *     PagedAttention).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * Layouts are row-major and contiguous; every pointer marked (device) is
+ * CUDA device memory (or managed memory) of the current device:
+ *   q, out          [num_seqs][num_q_heads][head_dim]                 T
+ *   k, v (new)      [num_tokens][num_kv_heads][head_dim]              T
+ *   k_cache,v_cache [num_blocks][block_size][num_kv_heads][head_dim]  T
+ *   block_tables    [num_seqs][max_blocks_per_seq]                    int32
+ *   context_lens    [num_seqs]                                        int32
+ *   slot_mapping    [num_tokens]                                      int64
+ * where T is fp16 or bf16 (pa_shape.dtype).  Query head h reads KV head
+ * h / (num_q_heads / num_kv_heads).  context_lens[b] counts every token of
+ * sequence b including the one just written; token i lives at offset
+ * i % block_size of physical block block_tables[b][i / block_size].
+ * Attention is softmax(scale * q . K^T) . V with fp32 accumulation; outputs
+ * are rounded to nearest-even into T.  An empty context gives zeros.
+ *
+ * Ownership: the caller owns every buffer, including split workspaces.  The
+ * library allocates nothing, frees nothing and never synchronises: work is
+ * enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ * default stream) and the call returns once it is enqueued.
+ *
+ * Errors: arguments are validated on the host before anything is enqueued;
+ * a failed check returns a non-zero pa_status and launches nothing.  A
+ * failed launch returns PA_ERR_CUDA (pa_last_cuda_error gives the code).
+ * Device-side values are bounded rather than trusted: a context length is
+ * clamped to [0, max_blocks_per_seq * block_size]; a physical block id
+ * outside [0, num_blocks) reads as zeros (never out of the pool); a slot
+ * outside the pool is skipped.  Those events, and any wait in a kernel that
+ * ran past its time limit, set bits of a device error word read with
+ * pa_read_device_errors.
+ *
+ * Supported shapes: head_dim 64 or 128; block_size 16 or 32; 1 <= num_q_heads /
+ * num_kv_heads <= 8; every device pointer 16-byte aligned.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, inconsistent shape */
+    PA_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, block_size, group */
+    PA_ERR_WORKSPACE = 3,     /* split workspace too small for the request */
+    PA_ERR_CUDA = 4           /* a CUDA call failed; see pa_last_cuda_error */
+} pa_status;
+
+typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Device error word bits (pa_read_device_errors). */
+#define PA_DEVERR_WAIT_TIMEOUT   0x1  /* a pipeline wait gave up after ~1 s */
+#define PA_DEVERR_BAD_CONTEXT    0x2  /* a context length was clamped */
+#define PA_DEVERR_BAD_SLOT       0x4  /* a slot past the pool was skipped */
+
+typedef struct {
+    int32_t num_seqs;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t max_blocks_per_seq;
+    int64_t num_blocks;
+    int32_t dtype;            /* pa_dtype */
+    int32_t reserved;         /* must be 0 */
+} pa_shape;
+
+/*
+ * reshape_and_cache: write each new token's K and V into its cache slot.
+ * For t < num_tokens with s = slot_mapping[t] (device):
+ *   s < 0                       -> padding, nothing written;
+ *   0 <= s < num_blocks*block_size
+ *       -> k_cache[s / block_size][s % block_size][:][:] = k[t][:][:],
+ *          v_cache likewise (bit copy);
+ *   otherwise                   -> skipped, PA_DEVERR_BAD_SLOT set.
+ * (youngju.dev post, PagedAttentionManager.append_token.)
+ * k, v, slot_mapping, k_cache, v_cache: device.  Uses shp->num_kv_heads,
+ * head_dim, block_size, num_blocks and dtype; num_seqs may differ from
+ * num_tokens and is ignored.  num_tokens == 0 enqueues nothing.
+ */
+int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                         void* k_cache, void* v_cache, int64_t num_tokens,
+                         const pa_shape* shp, void* stream);
+
+/*
+ * pa_decode: single-pass paged decode attention, one query token per sequence
+ * (ta-paperlens page, PagedAttention paragraph): for every b, h
+ *   out[b][h][:] = sum_i softmax_i(scale * q[b][h] . K_i) V_i,  i < context_lens[b].
+ * One CTA walks the whole context of a (sequence, KV head) and serves the
+ * group of query heads that share the KV head.
+ * q, k_cache, v_cache, block_tables, context_lens, out: device.
+ */
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale,
+              void* out, const pa_shape* shp, void* stream);
+
+/*
+ * Bytes of one contiguous split workspace for pa_decode_split / pa_reduce:
+ * [tmp_out][max_logits][exp_sums], each part rounded up to 256 bytes, with
+ * max_num_partitions = ceil(max_context_len / partition_size).
+ * Returns 0 for invalid arguments.
+ */
+size_t pa_split_workspace_size(const pa_shape* shp, int32_t max_context_len,
+                               int32_t partition_size);
+
+/*
+ * pa_decode_split: the context of each sequence is cut into partitions of
+ * partition_size tokens (a multiple of block_size); partition s covers
+ * tokens [s*P, min((s+1)*P, L_b)).  For each (b, h, s) with s*P < L_b and
+ * s < max_num_partitions it writes, in fp32:
+ *   max_logits[b][h][s]   = m_s = max_i scale * q . K_i
+ *   exp_sums[b][h][s]     = l_s = sum_i exp(scale * q . K_i - m_s)
+ *   tmp_out[b][h][s][:]   = sum_i exp(scale * q . K_i - m_s) V_i / l_s
+ * Partitions at or past the context end are not written.  Tokens at or past
+ * max_num_partitions * partition_size are not attended: the caller sizes
+ * max_num_partitions >= ceil(max_b L_b / partition_size).
+ * tmp_out [B][Hq][max_num_partitions][D], max_logits and exp_sums
+ * [B][Hq][max_num_partitions]: device, fp32, 16-byte aligned.
+ * (Context split and log-sum-exp merge are not in the pages; they follow
+ * the split-context decoding used for long contexts.)
+ */
+int pa_decode_split(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, float scale,
+                    int32_t partition_size, int32_t max_num_partitions,
+                    float* tmp_out, float* max_logits, float* exp_sums,
+                    const pa_shape* shp, void* stream);
+
+/*
+ * pa_reduce: log-sum-exp merge of pa_decode_split's partitions.  For each
+ * (b, h) with S_b = min(ceil(L_b / P), max_num_partitions):
+ *   M = max_s m_s,  w_s = l_s * exp(m_s - M),
+ *   out[b][h][:] = sum_s w_s tmp_out[b][h][s][:] / sum_s w_s   (zeros if S_b = 0).
+ * tmp_out, max_logits, exp_sums, context_lens, out: device.
+ */
+int pa_reduce(const float* tmp_out, const float* max_logits, const float* exp_sums,
+              const int32_t* context_lens, int32_t partition_size,
+              int32_t max_num_partitions, void* out, const pa_shape* shp, void* stream);
+
+/* Static description of a status code. */
+const char* pa_status_string(int status);
+
+/* cudaError_t of the most recent PA_ERR_CUDA on this host thread (0 if none). */
+int pa_last_cuda_error(void);
+
+/*
+ * Copy the device error word (PA_DEVERR_* bits accumulated by kernels of this
+ * library on the current device) to *flags, then clear it.  Synchronises
+ * `stream`.  Returns PA_OK or PA_ERR_CUDA.
+ */
+int pa_read_device_errors(int32_t* flags, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

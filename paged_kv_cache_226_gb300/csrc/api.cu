@@ -1,0 +1,289 @@
+// C-ABI entry points of libpa.so: host-side validation, TMA descriptor
+// encoding and kernel dispatch.  Declarations and contracts: include/pa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace {
+
+// Device error word (PA_DEVERR_* bits), one per device the library runs on.
+__device__ int g_device_errors;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices];
+std::mutex g_err_mutex;
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return PA_ERR_CUDA;
+}
+
+// Device address of the error word on the current device.
+cudaError_t error_word(int** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (g_err_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_errors);
+        if (e != cudaSuccess) return e;
+        g_err_ptr[dev] = static_cast<int*>(p);
+    }
+    *out = g_err_ptr[dev];
+    return cudaSuccess;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_status = cudaSuccess;
+
+cudaError_t get_encoder(EncodeTiledFn* fn) {
+    std::call_once(g_encode_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e == cudaSuccess && (q != cudaDriverEntryPointSuccess || p == nullptr))
+            e = cudaErrorSymbolNotFound;
+        g_encode_status = e;
+        g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    *fn = g_encode;
+    return g_encode_status;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Common shape checks.  Returns PA_OK or an error status.
+int check_shape(const pa_shape* s, bool need_q_heads) {
+    if (s == nullptr) return PA_ERR_INVALID_ARG;
+    if (s->reserved != 0) return PA_ERR_INVALID_ARG;
+    if (s->dtype != PA_FP16 && s->dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+    if (s->num_kv_heads <= 0 || s->head_dim <= 0 || s->block_size <= 0 || s->num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (s->head_dim != 64 && s->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (s->block_size != 16 && s->block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (s->num_blocks > 0xffffffffll) return PA_ERR_UNSUPPORTED;
+    if (need_q_heads) {
+        if (s->num_seqs < 0 || s->num_seqs > 65535) return PA_ERR_INVALID_ARG;
+        if (s->num_q_heads <= 0 || s->num_q_heads % s->num_kv_heads != 0)
+            return PA_ERR_INVALID_ARG;
+        if (s->num_q_heads / s->num_kv_heads > pa::kMaxGroup) return PA_ERR_UNSUPPORTED;
+        if (s->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+        if (s->max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+        if ((int64_t)s->max_blocks_per_seq * s->block_size > (1ll << 30)) return PA_ERR_UNSUPPORTED;
+    }
+    return PA_OK;
+}
+
+// 4-D view [num_blocks][block_size][Hkv][D] of a cache; box = 64 dims x one
+// head x 16 tokens x one block, 128 B swizzle (conflict-free ldmatrix rows).
+int encode_cache_map(CUtensorMap* map, const void* base, const pa_shape* s) {
+    EncodeTiledFn enc = nullptr;
+    cudaError_t e = get_encoder(&enc);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const cuuint64_t elem = 2;
+    cuuint64_t dims[4] = {(cuuint64_t)s->head_dim, (cuuint64_t)s->num_kv_heads,
+                          (cuuint64_t)s->block_size, (cuuint64_t)s->num_blocks};
+    cuuint64_t strides[3] = {s->head_dim * elem, (cuuint64_t)s->num_kv_heads * s->head_dim * elem,
+                             (cuuint64_t)s->block_size * s->num_kv_heads * s->head_dim * elem};
+    cuuint32_t box[4] = {(cuuint32_t)pa::kBoxElems, 1, (cuuint32_t)pa::kTileTokens, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUtensorMapDataType dt = s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int check_decode_args(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens,
+                      const pa_shape* shp) {
+    int st = check_shape(shp, true);
+    if (st != PA_OK) return st;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
+        !aligned16(context_lens))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+pa::DecodeParams make_params(const void* q, const int32_t* block_tables,
+                             const int32_t* context_lens, float scale, const pa_shape* shp,
+                             int* err) {
+    pa::DecodeParams p{};
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.err = err;
+    p.scale_log2 = scale * pa::kLog2e;
+    p.num_q_heads = shp->num_q_heads;
+    p.group = shp->num_q_heads / shp->num_kv_heads;
+    p.max_blocks_per_seq = shp->max_blocks_per_seq;
+    p.block_size = shp->block_size;
+    p.num_blocks = shp->num_blocks;
+    return p;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape";
+        case PA_ERR_WORKSPACE: return "split workspace too small";
+        case PA_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int pa_last_cuda_error(void) { return t_last_cuda_error; }
+
+int pa_read_device_errors(int32_t* flags, void* stream) {
+    if (flags == nullptr) return PA_ERR_INVALID_ARG;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    e = cudaMemcpyAsync(&host, err, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(err, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *flags = host;
+    return PA_OK;
+}
+
+int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                         void* k_cache, void* v_cache, int64_t num_tokens,
+                         const pa_shape* shp, void* stream) {
+    int st = check_shape(shp, false);
+    if (st != PA_OK) return st;
+    if (num_tokens < 0 || num_tokens > 0x7fffffffll) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int row_bytes = shp->num_kv_heads * shp->head_dim * 2;
+    e = pa::launch_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, num_tokens,
+                                     shp->num_blocks * shp->block_size, row_bytes, err,
+                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale,
+              void* out, const pa_shape* shp, void* stream) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!out || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp)) != PA_OK) return st;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err);
+    p.out = out;
+    dim3 grid(1, shp->num_kv_heads, shp->num_seqs);
+    e = pa::launch_decode(shp->dtype, shp->head_dim, false, tmk, tmv, p, grid,
+                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+size_t pa_split_workspace_size(const pa_shape* shp, int32_t max_context_len,
+                               int32_t partition_size) {
+    if (check_shape(shp, true) != PA_OK) return 0;
+    if (max_context_len < 0 || partition_size <= 0 || partition_size % shp->block_size != 0)
+        return 0;
+    const size_t parts = (size_t)((max_context_len + partition_size - 1) / partition_size);
+    const size_t rows = (size_t)shp->num_seqs * shp->num_q_heads * (parts ? parts : 1);
+    return round256(rows * shp->head_dim * sizeof(float)) + 2 * round256(rows * sizeof(float));
+}
+
+int pa_decode_split(const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, float scale,
+                    int32_t partition_size, int32_t max_num_partitions, float* tmp_out,
+                    float* max_logits, float* exp_sums, const pa_shape* shp, void* stream) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
+    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!tmp_out || !max_logits || !exp_sums) return PA_ERR_WORKSPACE;
+    if (!aligned16(tmp_out) || !aligned16(max_logits) || !aligned16(exp_sums))
+        return PA_ERR_INVALID_ARG;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp)) != PA_OK) return st;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err);
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.partition_tokens = partition_size;
+    p.max_parts = max_num_partitions;
+    dim3 grid(max_num_partitions, shp->num_kv_heads, shp->num_seqs);
+    e = pa::launch_decode(shp->dtype, shp->head_dim, true, tmk, tmv, p, grid,
+                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_reduce(const float* tmp_out, const float* max_logits, const float* exp_sums,
+              const int32_t* context_lens, int32_t partition_size, int32_t max_num_partitions,
+              void* out, const pa_shape* shp, void* stream) {
+    int st = check_shape(shp, true);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
+    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!tmp_out || !max_logits || !exp_sums) return PA_ERR_WORKSPACE;
+    if (!context_lens || !out || !aligned16(out) || !aligned16(tmp_out)) return PA_ERR_INVALID_ARG;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::ReduceParams p{};
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.context_lens = context_lens;
+    p.out = out;
+    p.err = err;
+    p.num_q_heads = shp->num_q_heads;
+    p.partition_tokens = partition_size;
+    p.max_parts = max_num_partitions;
+    p.max_context = shp->max_blocks_per_seq * shp->block_size;
+    e = pa::launch_reduce(shp->dtype, shp->head_dim, p, shp->num_seqs,
+                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,389 @@
+// Paged decode attention kernel for sm_103a.
+//
+// One CTA serves one (sequence b, KV head g[, context partition s]) and the
+// G = Hq/Hkv query heads that read KV head g.  It walks the sequence's block
+// table and gathers K and V while it computes (ta-paperlens "LLM serving
+// from scratch", section on fragmentation and PagedAttention).
+//
+// Data movement: a producer warp reads the block table and issues one TMA
+// box per 16-token half-row tile ([16 tokens][64 dims] of one KV head, 128 B
+// rows, 128 B swizzle) into an 8-stage shared-memory ring guarded by
+// mbarriers; a block of 32 tokens is two tiles.  Four consumer warps take the
+// tiles round robin.
+//
+// Math per tile and warp (the G <= 8 query heads of the group are the N = 8
+// columns of two m16n8k16 tile products; columns >= G are zero):
+//   S^T[t][h] = K[t] . q[h]            one product per 16 dims
+//   online softmax in log2 units with a lazily raised running max: the
+//   accumulator is rescaled only when a tile's column max exceeds the max in
+//   use by more than 2^8, so exp2(s - m) stays below 256 and fp32 is exact
+//   enough; the result is identical in exact arithmetic because numerator
+//   and denominator share the same reference max;
+//   P is rounded to the cache's 16-bit type (the row sum l accumulates the
+//   rounded values), transposed in registers with movmatrix, and
+//   O^T[d][h] += V^T[d][:] . P^T[:][h] with fp32 accumulation.
+// The four warps' (m, l, O) are merged through shared memory at the end.
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+// Rescale the accumulator only when the max grows by more than 2^8.
+constexpr float kRescaleThresholdLog2 = 8.0f;
+
+template <int D>
+struct DecodeLayout {
+    static constexpr int kHalves = D / kBoxElems;                 // boxes per tile
+    static constexpr int kBoxBytes = kTileTokens * kBoxElems * 2; // 2 KB
+    static constexpr int kTileBytes = kHalves * kBoxBytes;        // one of K or V
+    static constexpr int kStageBytes = 2 * kTileBytes;            // K and V
+    static constexpr int kPipeBytes = kStages * kStageBytes;
+    // merge area: per warp, O[8][D] then m_used[8], l[8], m_true[8]
+    static constexpr int kMergeFloatsPerWarp = kMaxGroup * D + 3 * kMaxGroup;
+    static constexpr int kMergeBytes = kConsumerWarps * kMergeFloatsPerWarp * 4;
+    static constexpr int kBodyBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+    static constexpr int kDynamicSmem = kBodyBytes + 1024;         // + alignment slack
+};
+
+template <typename T, int D, bool kSplit>
+__global__ void __launch_bounds__(kDecodeThreads, 3)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v,
+                        const __grid_constant__ DecodeParams p) {
+    using Lay = DecodeLayout<D>;
+    using M = Mma<T>;
+    constexpr int kKSteps = D / 16;     // 16-dim slices of D
+
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int g = blockIdx.y;
+    const int b = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = p.group;
+
+    // Context length, bounded so the table row is never overrun.
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    int L = p.context_lens[b];
+    if (L < 0 || L > max_ctx) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+        L = L < 0 ? 0 : max_ctx;
+    }
+    int t_begin = 0, t_end = L;
+    if (kSplit) {
+        t_begin = blockIdx.x * p.partition_tokens;
+        if (t_begin >= L) return;                       // partition past the end
+        t_end = min(t_begin + p.partition_tokens, L);
+    } else if (L == 0) {
+        // Empty context: zero output for the group's heads.
+        T* out = reinterpret_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)g * G) * D;
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = from_float<T>(0.f);
+        return;
+    }
+    const int tile_begin = t_begin / kTileTokens;                  // t_begin % 16 == 0
+    const int n_tiles = (t_end + kTileTokens - 1) / kTileTokens - tile_begin;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------------
+        // producer: block table -> TMA boxes
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            prefetch_tensor_map(&tmap_k);
+            prefetch_tensor_map(&tmap_v);
+        }
+        const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
+        const int tiles_per_block = p.block_size / kTileTokens;
+        bool ok = true;
+        for (int i0 = 0; i0 < n_tiles && ok; i0 += 32) {
+            const int mine = i0 + lane;
+            int blk = 0;
+            if (mine < n_tiles) {
+                blk = __ldg(table + (tile_begin + mine) / tiles_per_block);
+                if (blk < 0 || blk >= p.num_blocks) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+            }
+            const int cnt = min(32, n_tiles - i0);
+            for (int k = 0; k < cnt; ++k) {
+                const int pblk = __shfl_sync(0xffffffffu, blk, k);
+                if (lane == 0) {
+                    const int it = i0 + k;
+                    const int st = it % kStages;
+                    if (it >= kStages && !mbar_wait(&empty_bar[st], ((it / kStages) - 1) & 1)) {
+                        flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+                        ok = false;
+                    } else {
+                        mbar_arrive_expect_tx(&full_bar[st], Lay::kStageBytes);
+                        const int sub = ((tile_begin + it) % tiles_per_block) * kTileTokens;
+                        uint8_t* kdst = smem + st * Lay::kStageBytes;
+                        uint8_t* vdst = kdst + Lay::kTileBytes;
+#pragma unroll
+                        for (int hh = 0; hh < Lay::kHalves; ++hh) {
+                            tma_load_4d(kdst + hh * Lay::kBoxBytes, &tmap_k, &full_bar[st],
+                                        hh * kBoxElems, g, sub, pblk);
+                            tma_load_4d(vdst + hh * Lay::kBoxBytes, &tmap_v, &full_bar[st],
+                                        hh * kBoxElems, g, sub, pblk);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------------------
+    // consumers
+    // ----------------------------------------------------------------------
+    // Fragment roles (m16n8k16, r = lane/4, c = lane%4):
+    //   S^T[t][h] = K[t][:] . q[h][:]   A = K tile (16 tokens x 16 dims),
+    //                                   B = q^T (16 dims x 8 heads)
+    //   O^T[d][h] += V^T[d][:] . P^T[:][h]  A = V^T (16 dims x 16 tokens),
+    //                                   B = P^T (16 tokens x 8 heads)
+    // so each thread holds scores of tokens r and r+8 for heads 2c, 2c+1 and
+    // accumulators of dims r, r+8 (per 16-dim slab) for the same two heads.
+    const int r8 = lane >> 2;
+    const int c4 = lane & 3;
+    const int hA = 2 * c4, hB = 2 * c4 + 1;      // this thread's two heads
+
+    // q^T as the B operand: b0 = q[r8][16kk + 2c4 ..], b1 = q[r8][16kk + 8 + 2c4 ..]
+    uint32_t qb[kKSteps][2];
+    {
+        const bool qrow_valid = r8 < G;
+        const T* qrow = reinterpret_cast<const T*>(p.q) +
+                        ((size_t)b * p.num_q_heads + (size_t)g * G + (qrow_valid ? r8 : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk) {
+            qb[kk][0] = qrow_valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * c4)) : 0u;
+            qb[kk][1] = qrow_valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * c4)) : 0u;
+        }
+    }
+
+    float acc[kKSteps][4];      // O^T slabs of 16 dims
+#pragma unroll
+    for (int n = 0; n < kKSteps; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY;     // reference max in use (log2 units)
+    float tA = -INFINITY, tB = -INFINITY;     // true running max (log2 units)
+    float lA = 0.f, lB = 0.f;                 // this thread's share of the row sums
+
+    // ldmatrix row addresses: matrix j = lane/8 supplies row lane%8.
+    // K (A operand, no transpose): j -> (tokens 8*(j&1).., dims hi = j>>1)
+    const int k_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int k_hi = lane >> 4;
+    // V (A operand of V^T, transposed): j -> (tokens 8*(j>>1).., dims hi = j&1)
+    const int v_tok = (lane >> 4) * 8 + (lane & 7);
+    const int v_hi = (lane >> 3) & 1;
+
+    for (int it = warp; it < n_tiles; it += kConsumerWarps) {
+        const int st = it % kStages;
+        bool ok = mbar_wait(&full_bar[st], (it / kStages) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+            break;
+        }
+        uint8_t* ktile = smem + st * Lay::kStageBytes;
+        uint8_t* vtile = ktile + Lay::kTileBytes;
+        const uint32_t kbase = smem_u32(ktile);
+        const uint32_t vbase = smem_u32(vtile);
+
+        // S^T for the 16 tokens of the tile
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk) {
+            const int chunk = 2 * kk + k_hi;                 // 16-byte chunk along D
+            const uint32_t addr = kbase + (chunk >> 3) * Lay::kBoxBytes + k_tok * 128 +
+                                  (((chunk & 7) ^ (k_tok & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            M::run(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+
+        // mask past the span's end, scale into log2 units
+        const int tok0 = (tile_begin + it) * kTileTokens;
+        const bool v_lo = tok0 + r8 < t_end, v_hi8 = tok0 + r8 + 8 < t_end;
+        const float x0 = v_lo ? sc[0] * p.scale_log2 : -INFINITY;    // (r8,   hA)
+        const float x1 = v_lo ? sc[1] * p.scale_log2 : -INFINITY;    // (r8,   hB)
+        const float x2 = v_hi8 ? sc[2] * p.scale_log2 : -INFINITY;   // (r8+8, hA)
+        const float x3 = v_hi8 ? sc[3] * p.scale_log2 : -INFINITY;   // (r8+8, hB)
+        float xa = fmaxf(x0, x2), xb = fmaxf(x1, x3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
+            xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, o));
+        }
+        tA = fmaxf(tA, xa);
+        tB = fmaxf(tB, xb);
+        const bool raiseA = xa > mA + kRescaleThresholdLog2;
+        const bool raiseB = xb > mB + kRescaleThresholdLog2;
+        if (__any_sync(0xffffffffu, raiseA || raiseB)) {
+            const float nA = raiseA ? xa : mA, nB = raiseB ? xb : mB;
+            const float fA = ex2(mA - nA), fB = ex2(mB - nB);
+#pragma unroll
+            for (int n = 0; n < kKSteps; ++n) {
+                acc[n][0] *= fA;
+                acc[n][1] *= fB;
+                acc[n][2] *= fA;
+                acc[n][3] *= fB;
+            }
+            lA *= fA;
+            lB *= fB;
+            mA = nA;
+            mB = nB;
+        }
+        // P rounded to the cache type; P^T fragments by an in-register transpose
+        const uint32_t p01 = M::pack(ex2(x0 - mA), ex2(x1 - mB));   // token r8
+        const uint32_t p23 = M::pack(ex2(x2 - mA), ex2(x3 - mB));   // token r8+8
+        {
+            const float2 u = M::unpack(p01), w = M::unpack(p23);
+            lA += u.x + w.x;
+            lB += u.y + w.y;
+        }
+        const uint32_t pb0 = movmatrix_trans(p01);   // (head r8, tokens 2c4..+1)
+        const uint32_t pb1 = movmatrix_trans(p23);   // (head r8, tokens 8+2c4..+1)
+
+        // Ragged tail: V rows past the end may hold stale non-finite bits;
+        // zero them so that 0 * V stays 0 in the product below.
+        if (tok0 + kTileTokens > t_end) {
+            const int valid = t_end - tok0;
+            const int rows = kTileTokens - valid;
+            for (int idx = lane; idx < Lay::kHalves * rows * 8; idx += 32) {
+                const int hh = idx / (rows * 8);
+                const int rem = idx - hh * rows * 8;
+                const int rr = valid + (rem >> 3);
+                *reinterpret_cast<uint4*>(vtile + hh * Lay::kBoxBytes + rr * 128 + ((rem & 7) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // O^T += V^T . P^T, one m16n8k16 per 16-dim slab
+#pragma unroll
+        for (int n = 0; n < kKSteps; ++n) {
+            const int chunk = 2 * n + v_hi;
+            const uint32_t addr = vbase + (chunk >> 3) * Lay::kBoxBytes + v_tok * 128 +
+                                  (((chunk & 7) ^ (v_tok & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(addr, a0, a1, a2, a3);
+            M::run(acc[n], a0, a1, a2, a3, pb0, pb1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+
+    // row sums across the 8 lanes that share a head pair
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        lA += __shfl_xor_sync(0xffffffffu, lA, o);
+        lB += __shfl_xor_sync(0xffffffffu, lB, o);
+    }
+
+    // ----------------------------------------------------------------------
+    // merge the consumer warps
+    // ----------------------------------------------------------------------
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");   // pipeline drained
+    float* mrg = reinterpret_cast<float*>(smem);
+    {
+        float* wo = mrg + warp * Lay::kMergeFloatsPerWarp;
+#pragma unroll
+        for (int n = 0; n < kKSteps; ++n) {
+            const int d = 16 * n + r8;
+            if (hA < G) {
+                wo[hA * D + d] = acc[n][0];
+                wo[hA * D + d + 8] = acc[n][2];
+            }
+            if (hB < G) {
+                wo[hB * D + d] = acc[n][1];
+                wo[hB * D + d + 8] = acc[n][3];
+            }
+        }
+        if (r8 == 0) {
+            if (hA < G) {
+                wo[kMaxGroup * D + hA] = mA;
+                wo[kMaxGroup * D + kMaxGroup + hA] = lA;
+                wo[kMaxGroup * D + 2 * kMaxGroup + hA] = tA;
+            }
+            if (hB < G) {
+                wo[kMaxGroup * D + hB] = mB;
+                wo[kMaxGroup * D + kMaxGroup + hB] = lB;
+                wo[kMaxGroup * D + 2 * kMaxGroup + hB] = tB;
+            }
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+
+    const int tid = threadIdx.x;                      // 0..127
+    const int items = G * (D / 4);                    // 4 output dims per item
+    for (int item = tid; item < items; item += kConsumerWarps * 32) {
+        const int h = item / (D / 4);
+        const int d = (item - h * (D / 4)) * 4;
+        float mref = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+            mref = fmaxf(mref, mrg[w * Lay::kMergeFloatsPerWarp + kMaxGroup * D + h]);
+        float den = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f, mt = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float* wo = mrg + w * Lay::kMergeFloatsPerWarp;
+            const float mw = wo[kMaxGroup * D + h];
+            const float f = (mw == -INFINITY) ? 0.f : ex2(mw - mref);
+            den += f * wo[kMaxGroup * D + kMaxGroup + h];
+            const float4 v = *reinterpret_cast<const float4*>(wo + h * D + d);
+            o0 += f * v.x;
+            o1 += f * v.y;
+            o2 += f * v.z;
+            o3 += f * v.w;
+            mt = fmaxf(mt, wo[kMaxGroup * D + 2 * kMaxGroup + h]);
+        }
+        const float inv = 1.f / den;
+        const size_t qh = (size_t)b * p.num_q_heads + (size_t)g * G + h;
+        if (kSplit) {
+            const size_t idx = qh * p.max_parts + blockIdx.x;
+            *reinterpret_cast<float4*>(p.tmp_out + idx * D + d) =
+                make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
+            if (d == 0) {
+                p.max_logits[idx] = mt * kLn2;
+                p.exp_sums[idx] = den * ex2(mref - mt);
+            }
+        } else {
+            T* out = reinterpret_cast<T*>(p.out) + qh * D + d;
+            const uint32_t lo = M::pack(o0 * inv, o1 * inv);
+            const uint32_t hi = M::pack(o2 * inv, o3 * inv);
+            *reinterpret_cast<uint2*>(out) = make_uint2(lo, hi);
+        }
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_decode_t(bool split, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                            const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+    const int smem = DecodeLayout<D>::kDynamicSmem;
+    cudaError_t e;
+    if (split) {
+        e = cudaFuncSetAttribute(paged_decode_kernel<T, D, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        paged_decode_kernel<T, D, true><<<grid, kDecodeThreads, smem, stream>>>(tmk, tmv, p);
+    } else {
+        e = cudaFuncSetAttribute(paged_decode_kernel<T, D, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        paged_decode_kernel<T, D, false><<<grid, kDecodeThreads, smem, stream>>>(tmk, tmv, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pa

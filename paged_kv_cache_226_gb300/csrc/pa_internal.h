@@ -1,0 +1,64 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr int kTileTokens = 16;      // tokens per pipeline tile (one box row count)
+constexpr int kBoxElems = 64;        // innermost box extent: 64 x 2 B = one 128 B swizzle row
+constexpr int kConsumerWarps = 4;    // warps that compute; one more warp issues TMA
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 8;           // tiles in flight per CTA
+constexpr int kMaxGroup = 8;         // query heads per KV head served by one CTA
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct DecodeParams {
+    const void* q;                 // [B][Hq][D]
+    const int32_t* block_tables;   // [B][MB]
+    const int32_t* context_lens;   // [B]
+    void* out;                     // [B][Hq][D] (single pass)
+    float* tmp_out;                // [B][Hq][S][D] (split)
+    float* max_logits;             // [B][Hq][S]
+    float* exp_sums;               // [B][Hq][S]
+    int* err;                      // device error word
+    float scale_log2;              // scale * log2(e)
+    int num_q_heads;
+    int group;                     // Hq / Hkv
+    int max_blocks_per_seq;
+    int block_size;
+    int64_t num_blocks;
+    int partition_tokens;          // split: partition size; single pass: 0
+    int max_parts;                 // split: S
+};
+
+struct ReduceParams {
+    const float* tmp_out;
+    const float* max_logits;
+    const float* exp_sums;
+    const int32_t* context_lens;
+    void* out;
+    int* err;
+    int num_q_heads;
+    int partition_tokens;
+    int max_parts;
+    int max_context;               // max_blocks_per_seq * block_size (clamp bound)
+};
+
+// Kernel launchers (kernels live in their own translation units).
+cudaError_t launch_decode(int dtype, int head_dim, bool split, const CUtensorMap& tmk,
+                          const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
+                          cudaStream_t stream);
+cudaError_t launch_reduce(int dtype, int head_dim, const ReduceParams& p, int num_seqs,
+                          cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int64_t* slots,
+                                     void* kc, void* vc, int64_t num_tokens,
+                                     int64_t num_slots, int row_bytes, int* err,
+                                     cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,286 @@
+"""Python binding of libpa.so (the C ABI declared in include/pa.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  torch provides device memory and the current
+stream.  There is no fallback: if libpa.so is missing or cannot be loaded,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "pa.h")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_FP16, PA_BF16 = 0, 1
+PA_DEVERR_WAIT_TIMEOUT, PA_DEVERR_BAD_CONTEXT, PA_DEVERR_BAD_SLOT = 1, 2, 4
+DEFAULT_PARTITION = 512
+
+_DTYPE_CODES = {torch.float16: PA_FP16, torch.bfloat16: PA_BF16}
+
+
+class PaShape(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class PaError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status}){detail}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libpa.so (raises if it is absent: build it with
+    ``python -m paged_kv_cache_226_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"libpa.so not found at {p}; build it with "
+                              "`python -m paged_kv_cache_226_gb300.build`")
+        lib = ctypes.CDLL(p)
+        V, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        S = ctypes.POINTER(PaShape)
+        lib.pa_reshape_and_cache.argtypes = [V, V, V, V, V, I64, S, V]
+        lib.pa_decode.argtypes = [V, V, V, V, V, F, V, S, V]
+        lib.pa_split_workspace_size.argtypes = [S, I32, I32]
+        lib.pa_split_workspace_size.restype = ctypes.c_size_t
+        lib.pa_decode_split.argtypes = [V, V, V, V, V, F, I32, I32, V, V, V, S, V]
+        lib.pa_reduce.argtypes = [V, V, V, V, I32, I32, V, S, V]
+        lib.pa_status_string.argtypes = [ctypes.c_int]
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_last_cuda_error.argtypes = []
+        lib.pa_read_device_errors.argtypes = [ctypes.POINTER(I32), V]
+        for fn in ("pa_reshape_and_cache", "pa_decode", "pa_decode_split", "pa_reduce",
+                   "pa_last_cuda_error", "pa_read_device_errors"):
+            getattr(lib, fn).restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def header_symbols(header: str = HEADER_PATH):
+    """Names of the functions include/pa.h declares."""
+    with open(header) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != PA_OK:
+        detail = ""
+        if status == PA_ERR_CUDA:
+            detail = f", cudaError {load().pa_last_cuda_error()}"
+        raise PaError(fn, status, detail)
+
+
+def _stream_handle(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def make_shape(num_seqs: int, num_q_heads: int, k_cache: torch.Tensor,
+               max_blocks_per_seq: int) -> PaShape:
+    nb, bs, hkv, d = k_cache.shape
+    if k_cache.dtype not in _DTYPE_CODES:
+        raise TypeError(f"cache dtype must be float16 or bfloat16, got {k_cache.dtype}")
+    return PaShape(num_seqs=num_seqs, num_q_heads=num_q_heads, num_kv_heads=hkv, head_dim=d,
+                   block_size=bs, max_blocks_per_seq=max_blocks_per_seq, num_blocks=nb,
+                   dtype=_DTYPE_CODES[k_cache.dtype], reserved=0)
+
+
+def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                      k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """Write each new token's K/V ([T][Hkv][D]) into slot_mapping's cache slots."""
+    lib = load()
+    dev = k_cache.device
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_cache.dtype, dev)
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t, n, k_cache.dtype, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    T = slot_mapping.shape[0]
+    if k.shape != (T, k_cache.shape[2], k_cache.shape[3]) or v.shape != k.shape:
+        raise ValueError("k and v must be [num_tokens][num_kv_heads][head_dim]")
+    shp = make_shape(0, k_cache.shape[2], k_cache, 1)
+    _check("pa_reshape_and_cache",
+           lib.pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache),
+                                    _ptr(v_cache), T, ctypes.byref(shp), _stream_handle(dev)))
+
+
+def _decode_common(q, k_cache, v_cache, block_tables, context_lens):
+    dev = k_cache.device
+    _need(q, "q", k_cache.dtype, dev)
+    _need(k_cache, "k_cache", None, dev)
+    _need(v_cache, "v_cache", k_cache.dtype, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [num_blocks][block_size][num_kv_heads][head_dim]")
+    B, hq, d = q.shape
+    if d != k_cache.shape[3] or block_tables.dim() != 2 or block_tables.shape[0] != B \
+            or context_lens.shape != (B,):
+        raise ValueError("inconsistent q / block_tables / context_lens shapes")
+    return make_shape(B, hq, k_cache, block_tables.shape[1]), dev
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Single-pass paged decode attention (one CTA per sequence and KV head)."""
+    lib = load()
+    shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, dev)
+    _check("pa_decode", lib.pa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                      _ptr(context_lens), float(scale), _ptr(out),
+                                      ctypes.byref(shp), _stream_handle(dev)))
+    return out
+
+
+def num_partitions(max_context_len: int, partition_size: int = DEFAULT_PARTITION) -> int:
+    return max(1, -(-int(max_context_len) // int(partition_size)))
+
+
+def split_workspace(q: torch.Tensor, max_num_partitions: int
+                    ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Allocate (tmp_out, max_logits, exp_sums) for the split path."""
+    B, hq, d = q.shape
+    tmp = torch.empty((B, hq, max_num_partitions, d), dtype=torch.float32, device=q.device)
+    ml = torch.empty((B, hq, max_num_partitions), dtype=torch.float32, device=q.device)
+    es = torch.empty((B, hq, max_num_partitions), dtype=torch.float32, device=q.device)
+    return tmp, ml, es
+
+
+def workspace_size(num_seqs, num_q_heads, k_cache, max_blocks_per_seq, max_context_len,
+                   partition_size=DEFAULT_PARTITION) -> int:
+    shp = make_shape(num_seqs, num_q_heads, k_cache, max_blocks_per_seq)
+    return int(load().pa_split_workspace_size(ctypes.byref(shp), int(max_context_len),
+                                              int(partition_size)))
+
+
+def decode_split(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                 partition_size: int, max_num_partitions: int, tmp_out=None, max_logits=None,
+                 exp_sums=None):
+    """Per-partition outputs (tmp_out, max_logits, exp_sums) of the context split."""
+    lib = load()
+    shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    if tmp_out is None:
+        tmp_out, max_logits, exp_sums = split_workspace(q, max_num_partitions)
+    for t, n in ((tmp_out, "tmp_out"), (max_logits, "max_logits"), (exp_sums, "exp_sums")):
+        _need(t, n, torch.float32, dev)
+    B, hq, d = q.shape
+    if tmp_out.numel() < B * hq * max_num_partitions * d or \
+            max_logits.numel() < B * hq * max_num_partitions or \
+            exp_sums.numel() < B * hq * max_num_partitions:
+        raise PaError("pa_decode_split", PA_ERR_WORKSPACE)
+    _check("pa_decode_split",
+           lib.pa_decode_split(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                               _ptr(context_lens), float(scale), int(partition_size),
+                               int(max_num_partitions), _ptr(tmp_out), _ptr(max_logits),
+                               _ptr(exp_sums), ctypes.byref(shp), _stream_handle(dev)))
+    return tmp_out, max_logits, exp_sums
+
+
+def reduce(tmp_out, max_logits, exp_sums, context_lens, partition_size: int,
+           k_cache: torch.Tensor, max_blocks_per_seq: int, out: torch.Tensor) -> torch.Tensor:
+    """Log-sum-exp merge of decode_split's partitions into out [B][Hq][D]."""
+    lib = load()
+    dev = out.device
+    _need(out, "out", k_cache.dtype, dev)
+    for t, n in ((tmp_out, "tmp_out"), (max_logits, "max_logits"), (exp_sums, "exp_sums")):
+        _need(t, n, torch.float32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    B, hq, d = out.shape
+    S = tmp_out.shape[2]
+    shp = make_shape(B, hq, k_cache, max_blocks_per_seq)
+    _check("pa_reduce", lib.pa_reduce(_ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums),
+                                      _ptr(context_lens), int(partition_size), int(S), _ptr(out),
+                                      ctypes.byref(shp), _stream_handle(dev)))
+    return out
+
+
+def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                    max_context_len: int, out: Optional[torch.Tensor] = None,
+                    mode: str = "auto", partition_size: int = DEFAULT_PARTITION,
+                    workspace=None) -> torch.Tensor:
+    """Decode attention through the single-pass or the split + merge path.
+
+    ``mode="auto"`` splits when there are too few (sequence, KV head) pairs to
+    fill the GPU evenly or when contexts are long; ``max_context_len`` is the
+    host-known bound on ``context_lens`` (it sizes the split grid).
+    """
+    if out is None:
+        out = torch.empty_like(q)
+    if mode == "auto":
+        mode = choose_mode(q.shape[0], k_cache.shape[2], max_context_len, partition_size,
+                           q.device)
+    if mode == "single":
+        return decode(q, k_cache, v_cache, block_tables, context_lens, scale, out)
+    if mode != "split":
+        raise ValueError(f"unknown mode {mode!r}")
+    S = num_partitions(max_context_len, partition_size)
+    if workspace is None:
+        workspace = split_workspace(q, S)
+    tmp, ml, es = workspace
+    decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, partition_size, S,
+                 tmp, ml, es)
+    return reduce(tmp, ml, es, context_lens, partition_size, k_cache, block_tables.shape[1], out)
+
+
+def choose_mode(num_seqs: int, num_kv_heads: int, max_context_len: int, partition_size: int,
+                device=None) -> str:
+    """Single pass when every (sequence, KV head) CTA is short, else split."""
+    if max_context_len <= partition_size:
+        return "single"
+    return "split"
+
+
+def read_device_errors(device: Optional[torch.device] = None) -> int:
+    """Return and clear the library's device error word (PA_DEVERR_* bits)."""
+    lib = load()
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    flags = ctypes.c_int32(0)
+    with torch.cuda.device(dev):
+        _check("pa_read_device_errors",
+               lib.pa_read_device_errors(ctypes.byref(flags), _stream_handle(dev)))
+    return int(flags.value)

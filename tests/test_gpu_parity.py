@@ -1,0 +1,145 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU reference on
+the same seeded inputs.  Cache writes bit-exact; attention within
+|gpu - ref| <= 2e-3 + 1e-2 |ref| elementwise."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_226_gb300 import build, lib
+from paged_kv_cache_226_gb300 import inputs as pin
+from parity_util import assert_close, check_workload, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    lib.load()
+    d = torch.device("cuda:0")
+    lib.read_device_errors(d)
+    return d
+
+
+# ---------------------------------------------------------------------------
+# the named workloads at full size, both decode paths
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "prefix", "llama70b", "long16", "long32"])
+def test_named_workload(dev, name):
+    w = pin.build_workload(name)
+    errs = check_workload(w, dev)
+    print(name, errs)
+
+
+# ---------------------------------------------------------------------------
+# ragged edges: lengths around tile, block and partition boundaries
+# ---------------------------------------------------------------------------
+
+EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 511, 512, 513, 1024,
+             1100]
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs", [
+    ("fp16", 8, 2, 64, 16), ("bf16", 8, 2, 64, 32), ("fp16", 32, 8, 128, 16),
+    ("bf16", 64, 8, 128, 32), ("fp16", 4, 4, 128, 16), ("bf16", 2, 1, 64, 16),
+    ("fp16", 16, 8, 128, 32), ("bf16", 24, 4, 128, 16)])
+def test_edge_lengths(dev, dtype, hq, hkv, d, bs):
+    w = pin.build_workload(params=dict(dtype=dtype, num_seqs=len(EDGE_LENS), lens=EDGE_LENS,
+                                       num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                       block_size=bs), seed=hq * 7 + d + bs)
+    for P in sorted({bs, 2 * bs, 64 if 64 % bs == 0 else bs, 512}):
+        check_workload(w, dev, modes=("split",), partition_size=P)
+    check_workload(w, dev, modes=("single",))
+
+
+def test_single_partition_split_matches_single_pass(dev):
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=6, lens=[5, 16, 100, 300, 400, 512],
+                                       num_q_heads=16, num_kv_heads=4, head_dim=128,
+                                       block_size=16), seed=11)
+    d = to_device(w, dev)
+    single = lib.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                        w.scale)
+    split = lib.paged_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                d["context_lens"], w.scale, 512, mode="split")
+    assert_close(split.float().cpu().numpy(), single.float().cpu().numpy(),
+                 "split(1 partition) vs single", atol=1e-3, rtol=5e-3)
+
+
+# ---------------------------------------------------------------------------
+# cache contents the kernels must not depend on / must not touch
+# ---------------------------------------------------------------------------
+
+def test_stale_nan_past_context_end_is_ignored(dev):
+    """Slots past a sequence's end (inside its last block) hold NaN bits."""
+    w = pin.build_workload(params=dict(dtype="bf16", num_seqs=5, lens=[1, 7, 17, 250, 513],
+                                       num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                       block_size=32), seed=5)
+    kc = pin.bits(w.k_cache).copy()
+    vc = pin.bits(w.v_cache).copy()
+    for b in range(w.num_seqs):
+        L = int(w.context_lens[b])
+        last = w.block_tables[b, (L - 1) // w.block_size]
+        off = (L - 1) % w.block_size + 1
+        kc[last, off:] = 0x7fc0
+        vc[last, off:] = 0x7fc0
+    w.k_cache = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16)
+    w.v_cache = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16)
+    check_workload(w, dev, partition_size=64)
+
+
+def test_padding_and_out_of_pool_slots(dev):
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=4, lens=[3, 20, 40, 70],
+                                       num_q_heads=8, num_kv_heads=2, head_dim=64,
+                                       block_size=16), seed=9)
+    slots = w.slot_mapping.copy()
+    slots[1] = -1
+    w.slot_mapping = slots
+    check_workload(w, dev)                     # padding: nothing written, no error
+    d = to_device(w, dev)
+    before = d["k_cache"].clone()
+    far = torch.tensor([w.num_blocks * w.block_size + 7], dtype=torch.int64, device=dev)
+    lib.reshape_and_cache(d["k_new"][:1].contiguous(), d["v_new"][:1].contiguous(), far,
+                          d["k_cache"], d["v_cache"])
+    assert torch.equal(before, d["k_cache"])
+    assert lib.read_device_errors(dev) == lib.PA_DEVERR_BAD_SLOT
+    assert lib.read_device_errors(dev) == 0
+
+
+def test_context_longer_than_table_is_clamped_and_flagged(dev):
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=2, lens=[30, 64], num_q_heads=8,
+                                       num_kv_heads=2, head_dim=64, block_size=16), seed=4)
+    d = to_device(w, dev)
+    want = lib.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                      w.scale).clone()
+    assert lib.read_device_errors(dev) == 0
+    over = d["context_lens"].clone()
+    over[1] = 64 + 1000                      # table row holds 4 blocks = 64 tokens
+    got = lib.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], over, w.scale)
+    assert torch.equal(got, want)
+    assert lib.read_device_errors(dev) & lib.PA_DEVERR_BAD_CONTEXT
+
+
+def test_repeatable_bitwise(dev):
+    w = pin.build_workload("tiny")
+    d = to_device(w, dev)
+    outs = [lib.paged_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                d["context_lens"], w.scale, 250, mode=m).clone()
+            for m in ("single", "single", "split", "split")]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[2], outs[3])
+
+
+def test_non_default_stream(dev):
+    w = pin.build_workload("tiny")
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        d = to_device(w, dev)
+        out = lib.paged_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                  d["context_lens"], w.scale, 250, mode="split")
+    s.synchronize()
+    want = oracle.paged_decode(pin.bits(w.q), pin.bits(w.k_cache), pin.bits(w.v_cache),
+                               w.block_tables, w.context_lens, w.scale, w.dtype)
+    assert_close(out.float().cpu().numpy(), want, "side stream")
