@@ -94,9 +94,9 @@ def step_bytes(w: pin.Workload, mode: str, partition: int):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -110,7 +110,7 @@ class ClockSampler:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -125,50 +125,51 @@ class ClockSampler:
                 self.proc.kill()
         return False
 
-    def summary(self):
+    def summary(self, t0: float = None, t1: float = None):
+        """Median SM clock and the throttle reasons seen between wall times
+        t0 and t1 (time.time()); all samples when not given."""
         if self.proc is None or self.f is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        import datetime
         self.f.flush()
         self.f.seek(0)
         rows = [r.strip().split(", ") for r in self.f.read().splitlines() if r.strip()]
         os.unlink(self.f.name)
-        sm, smax, reasons = [], [], set()
+        sm, smax, reasons, n_all = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(r[2]), float(r[3])
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
+            n_all += 1
+            if t0 is not None and not (t0 - 0.03 <= ts <= t1 + 0.03):
+                continue
+            sm.append(clk)
+            smax.append(cmax)
+            for n, v in zip(names, r[6:10]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_total": n_all}
 
 
-def run_step(d, w, mode, partition, S, ws, out, evs=None, stream=None):
+def run_step(plan, evs=None, stream=None):
+    """One layer-step through the prepared C-ABI calls, with an event before,
+    between and after its kernels when ``evs`` is given."""
     if evs:
         evs[0].record(stream)
-    lib.reshape_and_cache(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"], d["v_cache"])
+    plan.reshape_and_cache()
     if evs:
         evs[1].record(stream)
-    if mode == "split":
-        tmp, ml, es = ws
-        lib.decode_split(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
-                         d["context_lens"], w.scale, partition, S, tmp, ml, es)
-        if evs:
-            evs[2].record(stream)
-        lib.reduce(tmp, ml, es, d["context_lens"], partition, d["k_cache"],
-                   w.max_blocks_per_seq, out)
-    else:
-        lib.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
-                   w.scale, out)
-        if evs:
-            evs[2].record(stream)
+    plan.decode()
+    if evs:
+        evs[2].record(stream)
+    plan.reduce()
     if evs:
         evs[3].record(stream)
 
@@ -271,15 +272,16 @@ def bench_ours(args):
         block_tables=torch.from_numpy(w.block_tables),
         context_lens=torch.from_numpy(w.context_lens),
         slot_mapping=torch.from_numpy(w.slot_mapping)).items()}
-    ws = lib.split_workspace(d["q"], S) if mode == "split" else None
-    out = torch.empty_like(d["q"])
+    plan = lib.StepPlan(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
+                        d["v_cache"], d["block_tables"], d["context_lens"], w.scale, max_len,
+                        mode=mode, partition_size=partition)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     nb = step_bytes(w, mode, partition)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        run_step(d, w, mode, partition, S, ws, out)
+        run_step(plan)
     torch.cuda.synchronize(dev)
     assert lib.read_device_errors(dev) == 0
 
@@ -289,13 +291,19 @@ def bench_ours(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local_rank) as clk:
-        time.sleep(0.3)
+        time.sleep(0.4)
+        t_epoch0 = time.time()
         t_wall = time.perf_counter()
+        # Hold the GPU briefly so the host queues the steps ahead of it: the
+        # events then see only GPU time, not Python launch overhead.
+        torch.cuda._sleep(int(2e7))
         for i in range(args.steps):
             flush.fill_(float(i))
-            run_step(d, w, mode, partition, S, ws, out, evs[i], stream)
+            run_step(plan, evs[i], stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
+        t_epoch1 = time.time()
+        time.sleep(0.1)
     if world > 1:
         dist.barrier()
     step_ms = [e[0].elapsed_time(e[3]) for e in evs]
@@ -309,35 +317,36 @@ def bench_ours(args):
         ms = float(t.item())
     errs = lib.read_device_errors(dev)
 
-    # end to end through the public API: pinned host inputs -> device, the
-    # layer-step, output -> host, every step
+    # End to end through the public API: every step copies its inputs from
+    # pinned host memory, runs the layer-step and reads the output back; the
+    # events bracket copies + kernels + the host's launch work (the L2 flush
+    # before each step is outside them).
     e2e = None
     if not args.no_e2e:
         host = {k: (torch.from_numpy(getattr(w, k)) if isinstance(getattr(w, k), np.ndarray)
                     else getattr(w, k)).pin_memory()
                 for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        out_h = torch.empty(plan.out.shape, dtype=plan.out.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_h.numel() * out_h.element_size()
-        for it in range(args.warmup + args.steps):
-            if it == args.warmup:
-                torch.cuda.synchronize(dev)
-                t0 = time.perf_counter()
+        n_e2e = min(args.steps, 200)
+        e_ms = []
+        for it in range(args.warmup + n_e2e):
             flush.fill_(0.5)
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
             for k, t in host.items():
                 d[k].copy_(t, non_blocking=True)
-            lib.reshape_and_cache(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
-                                  d["v_cache"])
-            lib.paged_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
-                                d["context_lens"], w.scale, max_len, out=out, mode=mode,
-                                partition_size=partition, workspace=ws)
-            out_h.copy_(out, non_blocking=True)
+            plan()
+            out_h.copy_(plan.out, non_blocking=True)
+            eb.record(stream)
             stream.synchronize()
-        e2e_s = (time.perf_counter() - t0) / args.steps
-        e2e = {"value": round(nb["layer_step"] * world / e2e_s / 1e9, 3), "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_s * 1e3, 4),
-               "note": "includes a 256 MiB L2-flush write per step"}
+            if it >= args.warmup:
+                e_ms.append(ea.elapsed_time(eb))
+        e2e_ms = sum(e_ms) / len(e_ms)
+        e2e = {"value": round(nb["layer_step"] * world / (e2e_ms * 1e-3) / 1e9, 3),
+               "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 5), "steps": n_e2e}
 
     if rank != 0:
         if world > 1:
@@ -374,7 +383,7 @@ def bench_ours(args):
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "traffic": profiled_traffic(args.config, dom)},
-        "clocks": clk.summary(),
+        "clocks": clk.summary(t_epoch0, t_epoch1),
         "gpu_launches": 3 * args.steps if mode == "split" else 2 * args.steps,
         "device_errors": errs,
         "wall_s_timed": round(t_wall, 4),
@@ -392,8 +401,8 @@ def bench_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama8b", choices=sorted(pin.CONFIGS))
     ap.add_argument("--mode", default="auto", choices=["auto", "single", "split"])

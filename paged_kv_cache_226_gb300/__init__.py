@@ -7,5 +7,5 @@ block allocator and seeded workload builder.
 from . import inputs  # noqa: F401
 from .lib import (  # noqa: F401
     DEFAULT_PARTITION, PaError, decode, decode_split, load, num_partitions, paged_attention,
-    read_device_errors, reduce, reshape_and_cache, split_workspace,
+    StepPlan, read_device_errors, reduce, reshape_and_cache, split_workspace,
 )

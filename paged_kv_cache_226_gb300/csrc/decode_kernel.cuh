@@ -19,11 +19,14 @@
 //   use by more than 2^8, so exp2(s - m) stays below 256 and fp32 is exact
 //   enough; the result is identical in exact arithmetic because numerator
 //   and denominator share the same reference max;
-//   P is rounded to the cache's 16-bit type (the row sum l accumulates the
-//   rounded values), transposed in registers with movmatrix, and
-//   O^T[d][h] += V^T[d][:] . P^T[:][h] with fp32 accumulation.
+//   P is rounded to the cache's 16-bit type -- for fp16 once (the row sum l
+//   accumulates the rounded values), for bf16 as a hi + lo pair of bf16
+//   values whose sum carries P to ~2^-17 -- transposed in registers with
+//   movmatrix, and O^T[d][h] += V^T[d][:] . P^T[:][h] with fp32 accumulation.
 // The four warps' (m, l, O) are merged through shared memory at the end.
 #pragma once
+
+#include <type_traits>
 
 #include "pa_device.cuh"
 
@@ -54,6 +57,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     using Lay = DecodeLayout<D>;
     using M = Mma<T>;
     constexpr int kKSteps = D / 16;     // 16-dim slices of D
+    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
 
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -243,16 +247,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
             mA = nA;
             mB = nB;
         }
-        // P rounded to the cache type; P^T fragments by an in-register transpose
-        const uint32_t p01 = M::pack(ex2(x0 - mA), ex2(x1 - mB));   // token r8
-        const uint32_t p23 = M::pack(ex2(x2 - mA), ex2(x3 - mB));   // token r8+8
-        {
+        // P in the cache's 16-bit type; P^T fragments by an in-register
+        // transpose.  fp16 keeps P to 2^-11; for bf16 P = hi + lo (two bf16
+        // parts, ~2^-17 together) and the product below runs once per part.
+        const float e0 = ex2(x0 - mA), e1 = ex2(x1 - mB);   // token r8
+        const float e2 = ex2(x2 - mA), e3 = ex2(x3 - mB);   // token r8+8
+        const uint32_t p01 = M::pack(e0, e1);
+        const uint32_t p23 = M::pack(e2, e3);
+        const uint32_t pb0 = movmatrix_trans(p01);   // (head r8, tokens 2c4..+1)
+        const uint32_t pb1 = movmatrix_trans(p23);   // (head r8, tokens 8+2c4..+1)
+        uint32_t pl0 = 0u, pl1 = 0u;
+        if (kSplitP) {
+            const float2 u = M::unpack(p01), w = M::unpack(p23);
+            pl0 = movmatrix_trans(M::pack(e0 - u.x, e1 - u.y));
+            pl1 = movmatrix_trans(M::pack(e2 - w.x, e3 - w.y));
+            lA += e0 + e2;
+            lB += e1 + e3;
+        } else {
             const float2 u = M::unpack(p01), w = M::unpack(p23);
             lA += u.x + w.x;
             lB += u.y + w.y;
         }
-        const uint32_t pb0 = movmatrix_trans(p01);   // (head r8, tokens 2c4..+1)
-        const uint32_t pb1 = movmatrix_trans(p23);   // (head r8, tokens 8+2c4..+1)
 
         // Ragged tail: V rows past the end may hold stale non-finite bits;
         // zero them so that 0 * V stays 0 in the product below.
@@ -279,6 +294,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
             uint32_t a0, a1, a2, a3;
             ldsm_x4_trans(addr, a0, a1, a2, a3);
             M::run(acc[n], a0, a1, a2, a3, pb0, pb1);
+            if (kSplitP) M::run(acc[n], a0, a1, a2, a3, pl0, pl1);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);

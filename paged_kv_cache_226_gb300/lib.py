@@ -284,3 +284,109 @@ def read_device_errors(device: Optional[torch.device] = None) -> int:
         _check("pa_read_device_errors",
                lib.pa_read_device_errors(ctypes.byref(flags), _stream_handle(dev)))
     return int(flags.value)
+
+
+class StepPlan:
+    """One decode layer-step with its arguments marshalled once.
+
+    Holds the C-ABI argument lists of reshape_and_cache, the decode kernel
+    (single pass, or split + merge) for fixed tensors, so that each launch
+    costs one ctypes call.  The work goes to the caller's current stream at
+    call time, which also makes a step capturable into a CUDA graph
+    (``capture_graph``).  The tensors must stay alive and keep their shapes;
+    their contents (new tokens, tables, lengths) may change between steps as
+    long as ``context_lens`` stays within ``max_context_len``.
+    """
+
+    def __init__(self, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                 context_lens, scale: float, max_context_len: int, out=None,
+                 mode: str = "auto", partition_size: int = DEFAULT_PARTITION, workspace=None):
+        self._lib = load()
+        shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+            _need(t, n, k_cache.dtype, dev)
+        _need(slot_mapping, "slot_mapping", torch.int64, dev)
+        T = slot_mapping.shape[0]
+        if k_new.shape != (T, k_cache.shape[2], k_cache.shape[3]) or v_new.shape != k_new.shape:
+            raise ValueError("k_new and v_new must be [num_tokens][num_kv_heads][head_dim]")
+        self.device = dev
+        self.out = torch.empty_like(q) if out is None else out
+        _need(self.out, "out", q.dtype, dev)
+        if mode == "auto":
+            mode = choose_mode(q.shape[0], k_cache.shape[2], max_context_len, partition_size)
+        if mode not in ("single", "split"):
+            raise ValueError(f"unknown mode {mode!r}")
+        self.mode = mode
+        self.partition_size = int(partition_size)
+        self.num_partitions = num_partitions(max_context_len, partition_size)
+        self._shape = shp
+        self._keep = [q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                      context_lens, self.out]
+        sref = ctypes.byref(self._shape)
+        self._reshape_args = (_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache),
+                              _ptr(v_cache), ctypes.c_int64(T), sref)
+        if mode == "single":
+            self._decode_args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                 _ptr(context_lens), ctypes.c_float(scale), _ptr(self.out), sref)
+        else:
+            if workspace is None:
+                workspace = split_workspace(q, self.num_partitions)
+            tmp, ml, es = workspace
+            B, hq, d = q.shape
+            if tmp.numel() < B * hq * self.num_partitions * d or \
+                    ml.numel() < B * hq * self.num_partitions or \
+                    es.numel() < B * hq * self.num_partitions:
+                raise PaError("pa_decode_split", PA_ERR_WORKSPACE)
+            self.workspace = workspace
+            self._keep += list(workspace)
+            S = ctypes.c_int32(self.num_partitions)
+            P = ctypes.c_int32(self.partition_size)
+            self._decode_args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                 _ptr(context_lens), ctypes.c_float(scale), P, S, _ptr(tmp),
+                                 _ptr(ml), _ptr(es), sref)
+            self._reduce_args = (_ptr(tmp), _ptr(ml), _ptr(es), _ptr(context_lens), P, S,
+                                 _ptr(self.out), sref)
+        self._graph = None
+
+    def _stream(self):
+        return ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
+
+    def reshape_and_cache(self):
+        _check("pa_reshape_and_cache",
+               self._lib.pa_reshape_and_cache(*self._reshape_args, self._stream()))
+
+    def decode(self):
+        if self.mode == "single":
+            _check("pa_decode", self._lib.pa_decode(*self._decode_args, self._stream()))
+        else:
+            _check("pa_decode_split",
+                   self._lib.pa_decode_split(*self._decode_args, self._stream()))
+
+    def reduce(self):
+        if self.mode == "split":
+            _check("pa_reduce", self._lib.pa_reduce(*self._reduce_args, self._stream()))
+
+    def __call__(self) -> torch.Tensor:
+        self.reshape_and_cache()
+        self.decode()
+        self.reduce()
+        return self.out
+
+    def capture_graph(self) -> "torch.cuda.CUDAGraph":
+        """Capture one step into a CUDA graph (replayed by ``replay``)."""
+        s = torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):
+            self()                                   # warm the lazy set-up outside capture
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self()
+        self._graph = g
+        return g
+
+    def replay(self) -> torch.Tensor:
+        if self._graph is None:
+            self.capture_graph()
+        self._graph.replay()
+        return self.out

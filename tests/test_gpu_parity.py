@@ -143,3 +143,29 @@ def test_non_default_stream(dev):
     want = oracle.paged_decode(pin.bits(w.q), pin.bits(w.k_cache), pin.bits(w.v_cache),
                                w.block_tables, w.context_lens, w.scale, w.dtype)
     assert_close(out.float().cpu().numpy(), want, "side stream")
+
+
+@pytest.mark.parametrize("mode", ["single", "split"])
+def test_step_plan_eager_and_graph_replay(dev, mode):
+    """The prepared step (and its CUDA-graph replay) equals the plain calls."""
+    w = pin.build_workload(params=dict(dtype="bf16", num_seqs=9, lens=[1, 16, 33, 100, 600, 1000,
+                                                                      1500, 2047, 2048],
+                                       num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                       block_size=16), seed=21)
+    d = to_device(w, dev)
+    plan = lib.StepPlan(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
+                        d["v_cache"], d["block_tables"], d["context_lens"], w.scale, 2048,
+                        mode=mode)
+    eager = plan().clone()
+    kc, vc, _ = oracle.reshape_and_cache(pin.bits(w.k_new), pin.bits(w.v_new), w.slot_mapping,
+                                         pin.bits(w.k_cache), pin.bits(w.v_cache), w.block_size)
+    want = oracle.paged_decode(pin.bits(w.q), kc, vc, w.block_tables, w.context_lens, w.scale,
+                               w.dtype)
+    assert_close(eager.float().cpu().numpy(), want, f"plan {mode}")
+    plan.out.zero_()
+    plan.capture_graph()
+    for _ in range(3):
+        got = plan.replay()
+    torch.cuda.synchronize(dev)
+    assert torch.equal(got, eager)
+    assert lib.read_device_errors(dev) == 0
