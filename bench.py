@@ -46,6 +46,26 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def rank_seed(config: str, rank: int) -> int:
+    """Each rank draws its own batch of the same shape (weak scaling)."""
+    return pin.CONFIGS[config][0] + 1000 * rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """MAX of a per-rank scalar over the process group (identity without one)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """All ranks' bytes per step over the slowest rank's step time."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -259,8 +279,7 @@ def bench_ours(args):
     pa_build.build()
     lib.load()
 
-    seed = pin.CONFIGS[args.config][0] + 1000 * rank
-    w = pin.build_workload(args.config, seed=seed)
+    w = pin.build_workload(args.config, seed=rank_seed(args.config, rank))
     max_len = int(w.context_lens.max())
     mode = args.mode if args.mode != "auto" else lib.choose_mode(
         w.num_seqs, w.num_kv_heads, max_len, args.partition)
@@ -310,11 +329,7 @@ def bench_ours(args):
     k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
     k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
     k3_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
     errs = lib.read_device_errors(dev)
 
     # End to end through the public API: every step copies its inputs from
@@ -343,8 +358,8 @@ def bench_ours(args):
             stream.synchronize()
             if it >= args.warmup:
                 e_ms.append(ea.elapsed_time(eb))
-        e2e_ms = sum(e_ms) / len(e_ms)
-        e2e = {"value": round(nb["layer_step"] * world / (e2e_ms * 1e-3) / 1e9, 3),
+        e2e_ms = max_over_ranks(sum(e_ms) / len(e_ms), dev)
+        e2e = {"value": round(whole_job_gbs(nb["layer_step"], world, e2e_ms), 3),
                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 5), "steps": n_e2e}
 
@@ -358,7 +373,7 @@ def bench_ours(args):
     dom_ms = sum(k2_ms) / len(k2_ms)
     dom_bytes = nb["kernels"][dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    value = nb["layer_step"] * world / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(nb["layer_step"], world, ms)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)

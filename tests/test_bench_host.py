@@ -1,0 +1,56 @@
+"""Host logic of the multi-rank bench path, run as two gloo ranks on CPU:
+per-rank batches differ but share a shape, the step time is the MAX over
+ranks, and the whole-job value counts every rank's bytes."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        from paged_kv_cache_226_gb300 import inputs as pin
+        w = pin.build_workload("tiny", seed=bench.rank_seed("tiny", rank))
+        local_ms = 1.0 + rank                      # rank 1 is the slow one
+        ms = bench.max_over_ranks(local_ms)
+        q.put((rank, ms, int(w.context_lens.sum()), w.q.shape, float(w.q.float().sum()),
+               bench.dist_env()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_timing_and_sharding():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, ms0, n0, s0, q0, env0), (r1, ms1, n1, s1, q1, env1) = res
+    assert ms0 == ms1 == 2.0                      # MAX over ranks on both
+    assert s0 == s1 and n0 == n1                  # same shape (tiny has fixed lengths)
+    assert q0 != q1                               # different draws per rank
+    assert env0 == (0, 2, 0) and env1 == (1, 2, 1)
+
+
+def test_whole_job_value_counts_all_ranks():
+    import bench
+    assert bench.whole_job_gbs(1_000_000_000, 4, 2.0) == pytest.approx(2000.0)
+    assert bench.max_over_ranks(3.5) == 3.5       # no process group: identity
