@@ -156,6 +156,48 @@ int pa_reduce(const float* tmp_out, const float* max_logits, const float* exp_su
               const int32_t* context_lens, int32_t partition_size,
               int32_t max_num_partitions, void* out, const pa_shape* shp, void* stream);
 
+/*
+ * Size of the device buffer behind pa_decode_static_workspace: 32 MiB,
+ * held on every GPU that loads the library until the process exits.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/*
+ * pa_decode_static_workspace: pa_decode_split followed by pa_reduce, with the
+ * partition workspace (tmp_out, max_logits, exp_sums) taken from a fixed
+ * device buffer inside the library instead of from the caller.  It allocates
+ * nothing.  The pages have no counterpart: this entry point exists for
+ * callers that cannot allocate device memory -- code running inside a host
+ * framework that owns the device memory pool (a private cudaMalloc would
+ * bypass the pool and may fail once the pool holds the free memory), or a
+ * latency-critical loop that cannot take the device-wide synchronisation of
+ * cudaMalloc / cudaFree.  The caller passes its inputs and `out` exactly as
+ * for pa_decode_split + pa_reduce (same layouts, same device pointers,
+ * partition_size a multiple of block_size, max_num_partitions >=
+ * ceil(max_b L_b / partition_size)); out [B][Hq][D] receives the merged
+ * attention output.
+ *
+ * Limit: the workspace, laid out [tmp_out][max_logits][exp_sums] with each
+ * part rounded up to 256 bytes (4*B*Hq*S*D, then 4*B*Hq*S twice), must fit in
+ * PA_STATIC_WORKSPACE_BYTES; larger requests return PA_ERR_WORKSPACE and
+ * enqueue nothing.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * buffer's device address; make that first call before any stream capture.
+ *
+ * Sharing: every call on a device uses the same buffer, which keeps the last
+ * call's contents (nothing in it needs to start at zero).  Calls whose work
+ * overlaps on the GPU -- e.g. issued on two streams without ordering between
+ * them -- race on the buffer and corrupt each other's results; order them.
+ * Errors are those of pa_decode_split and pa_reduce, plus PA_ERR_WORKSPACE
+ * for the limit above.
+ */
+int pa_decode_static_workspace(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               float scale, int32_t partition_size,
+                               int32_t max_num_partitions, void* out, const pa_shape* shp,
+                               void* stream);
+
 /* Static description of a status code. */
 const char* pa_status_string(int status);
 

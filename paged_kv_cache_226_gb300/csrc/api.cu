@@ -144,6 +144,8 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
+void pa::record_cuda_error(int cuda_error) { t_last_cuda_error = cuda_error; }
+
 extern "C" {
 
 const char* pa_status_string(int status) {

@@ -61,4 +61,7 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int64_t
                                      int64_t num_slots, int row_bytes, int* err,
                                      cudaStream_t stream);
 
+// Sets the value pa_last_cuda_error() reports on this host thread.
+void record_cuda_error(int cuda_error);
+
 }  // namespace pa

@@ -65,6 +65,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pa_split_workspace_size.restype = ctypes.c_size_t
         lib.pa_decode_split.argtypes = [V, V, V, V, V, F, I32, I32, V, V, V, S, V]
         lib.pa_reduce.argtypes = [V, V, V, V, I32, I32, V, S, V]
+        lib.pa_decode_static_workspace.argtypes = [V, V, V, V, V, F, I32, I32, V, S, V]
+        lib.pa_decode_static_workspace.restype = ctypes.c_int
         lib.pa_status_string.argtypes = [ctypes.c_int]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_last_cuda_error.argtypes = []
@@ -265,6 +267,32 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: floa
     decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, partition_size, S,
                  tmp, ml, es)
     return reduce(tmp, ml, es, context_lens, partition_size, k_cache, block_tables.shape[1], out)
+
+
+STATIC_WORKSPACE_BYTES = 32 << 20
+
+
+def decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                            max_context_len: int, out: Optional[torch.Tensor] = None,
+                            partition_size: int = DEFAULT_PARTITION) -> torch.Tensor:
+    """Split decode + merge using the library's own fixed device buffer for
+    the partition workspace (pa_decode_static_workspace): for callers that
+    must not allocate device memory, e.g. inside a framework that owns the
+    device memory pool.  ``out`` must be given by such callers (allocating it
+    here is a convenience for tests).  Calls that overlap on the GPU share
+    the buffer and race; keep them ordered."""
+    lib = load()
+    shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, dev)
+    S = num_partitions(max_context_len, partition_size)
+    _check("pa_decode_static_workspace",
+           lib.pa_decode_static_workspace(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(block_tables), _ptr(context_lens), float(scale),
+                                          int(partition_size), int(S), _ptr(out),
+                                          ctypes.byref(shp), _stream_handle(dev)))
+    return out
 
 
 def choose_mode(num_seqs: int, num_kv_heads: int, max_context_len: int, partition_size: int,
