@@ -4,8 +4,9 @@
 One step = one decode layer-step of the whole batch: reshape_and_cache of the
 new token of every sequence, then decode attention through the block tables
 (split kernel + log-sum-exp merge, or the single pass).  Inputs are seeded
-synthetic workloads resident in HBM; L2 is flushed (a 256 MiB write) before
-every step and only the step's own kernels sit between its CUDA events.
+synthetic workloads resident in HBM; L2 is flushed before
+every step (a 256 MiB write, then a 256 MiB read) and only the step's own
+kernels sit between its CUDA events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama8b]
     python bench.py --impl reference ...   # the CPU reference on host cores
@@ -178,6 +179,23 @@ class ClockSampler:
                 "samples": len(sm), "samples_total": n_all}
 
 
+class L2Flush:
+    """Evicts the 129 MB L2 between steps: writes one 256 MiB buffer, then
+    reads another, so that the step starts with L2 holding only clean lines
+    of the second buffer (no write-back of dirty flush data is left for the
+    step's own kernels to pay for)."""
+
+    def __init__(self, dev):
+        n = L2_FLUSH_BYTES // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.ones(n, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, value: float):
+        self.w.fill_(value)
+        torch.sum(self.r, dim=(0,), out=self.sink)
+
+
 def run_step(plan, evs=None, stream=None):
     """One layer-step through the prepared C-ABI calls, with an event before,
     between and after its kernels when ``evs`` is given."""
@@ -213,6 +231,17 @@ def cpu_baseline(w: pin.Workload, budget_s: float = 12.0):
             "kind": "oracle",
             "sample": f"{passes} full pass(es) of the {w.name} workload (reshape_and_cache + fp64 "
                       f"paged decode of all {w.num_seqs} sequences), {el:.1f} s"}
+
+
+def make_workload(args, rank: int) -> pin.Workload:
+    """The named workload, with --params (JSON) overriding its parameters."""
+    if not args.params:
+        return pin.build_workload(args.config, seed=rank_seed(args.config, rank))
+    seed, params = pin.CONFIGS[args.config]
+    params = dict(params, **json.loads(args.params))
+    w = pin.build_workload(args.config, seed=seed + 1000 * rank, params=params)
+    w.name = args.config
+    return w
 
 
 def bench_reference(args):
@@ -279,7 +308,7 @@ def bench_ours(args):
     pa_build.build()
     lib.load()
 
-    w = pin.build_workload(args.config, seed=rank_seed(args.config, rank))
+    w = make_workload(args, rank)
     max_len = int(w.context_lens.max())
     mode = args.mode if args.mode != "auto" else lib.choose_mode(
         w.num_seqs, w.num_kv_heads, max_len, args.partition)
@@ -294,17 +323,24 @@ def bench_ours(args):
     plan = lib.StepPlan(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
                         d["v_cache"], d["block_tables"], d["context_lens"], w.scale, max_len,
                         mode=mode, partition_size=partition)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     nb = step_bytes(w, mode, partition)
 
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush(1.0)
         run_step(plan)
     torch.cuda.synchronize(dev)
     assert lib.read_device_errors(dev) == 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # Timed region.  Phase 1 (the K timed steps): events only at step
+    # boundaries, so consecutive kernels of a step overlap their launch
+    # latency (programmatic dependent launch).  Phase 2 (kernel attribution,
+    # min(K, 1000) more steps): events between the kernels as well, which
+    # serialises them, to time each kernel for the roofline.
+    n_attr = min(args.steps, 1000)
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_attr)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -317,18 +353,26 @@ def bench_ours(args):
         # events then see only GPU time, not Python launch overhead.
         torch.cuda._sleep(int(2e7))
         for i in range(args.steps):
-            flush.fill_(float(i))
-            run_step(plan, evs[i], stream)
+            flush(float(i))
+            step_ev[i][0].record(stream)
+            run_step(plan)
+            step_ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
+        torch.cuda._sleep(int(2e7))
+        for i in range(n_attr):
+            flush(float(i))
+            run_step(plan, evs[i], stream)
+        torch.cuda.synchronize(dev)
         t_epoch1 = time.time()
         time.sleep(0.1)
     if world > 1:
         dist.barrier()
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[1]) for e in step_ev]
     k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
     k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
     k3_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    serial_ms = sum(e[0].elapsed_time(e[3]) for e in evs) / n_attr
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
     errs = lib.read_device_errors(dev)
 
@@ -347,7 +391,7 @@ def bench_ours(args):
         n_e2e = min(args.steps, 200)
         e_ms = []
         for it in range(args.warmup + n_e2e):
-            flush.fill_(0.5)
+            flush(0.5)
             ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ea.record(stream)
             for k, t in host.items():
@@ -385,13 +429,17 @@ def bench_ours(args):
             round(value / world / hbm, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
-        "config": {"workload": f"{w.name}: {pin.DESCRIPTIONS[w.name]}", "mode": mode,
+        "config": {"workload": f"{w.name}: {pin.DESCRIPTIONS[w.name]}"
+                               + (f" with {args.params}" if args.params else ""), "mode": mode,
                    "partition_tokens": partition if mode == "split" else None,
-                   "l2": "flushed before every step (256 MiB write, outside the step's events)",
+                   "l2": "flushed before every step (256 MiB write, then 256 MiB read of another "
+                         "buffer; outside the step's events)",
                    "kv_bytes": w.kv_bytes_logical(), "kv_bytes_unique": w.kv_bytes_unique(),
                    "bytes_per_step": nb["layer_step"], "seqs_per_gpu": w.num_seqs},
         "kernels_us": {"reshape_and_cache": round(1e3 * sum(k1_ms) / len(k1_ms), 2),
-                       dom: round(1e3 * dom_ms, 2)},
+                       dom: round(1e3 * dom_ms, 2),
+                       "note": f"event-bracketed, serialised, over {n_attr} more steps; the "
+                               f"same step serialised takes {1e3 * serial_ms:.2f} us"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2),
                      "peak": hbm, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
@@ -422,6 +470,7 @@ def main(argv=None):
     ap.add_argument("--config", default="llama8b", choices=sorted(pin.CONFIGS))
     ap.add_argument("--mode", default="auto", choices=["auto", "single", "split"])
     ap.add_argument("--partition", type=int, default=lib.DEFAULT_PARTITION)
+    ap.add_argument("--params", default="", help="JSON overrides of the workload parameters")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(256)
                              const int64_t* __restrict__ slots, uint4* __restrict__ kc,
                              uint4* __restrict__ vc, int64_t num_slots, int vec_per_row,
                              int* err) {
+    grid_dependency_wait();
+    allow_dependent_launch();
     const int64_t t = blockIdx.x;
     const int64_t s = slots[t];
     if (s < 0) return;                                  // padding token
@@ -53,10 +55,10 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int64_t
                                      cudaStream_t stream) {
     const int vec = row_bytes / 16;
     int threads = vec < 256 ? ((vec + 31) / 32) * 32 : 256;
-    reshape_and_cache_kernel<<<dim3((unsigned)num_tokens), threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
-        static_cast<uint4*>(kc), static_cast<uint4*>(vc), num_slots, vec, err);
-    return cudaGetLastError();
+    return launch_with_pdl(reshape_and_cache_kernel, dim3((unsigned)num_tokens), dim3(threads), 0,
+                           stream, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                           slots, static_cast<uint4*>(kc), static_cast<uint4*>(vc), num_slots,
+                           vec, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -65,65 +67,113 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int64_t
 //
 // For (b, h): S = min(ceil(L/P), max_parts) partitions with normalised
 // outputs o_s, maxima m_s and sums l_s.  M = max m_s, w_s = l_s e^(m_s - M),
-// out = sum w_s o_s / sum w_s.  One CTA of D threads per (b, h); thread d
-// owns output dim d; the m_s / l_s reads are warp-broadcast.
+// out = sum w_s o_s / sum w_s.  One CTA of 8 warps per (b, h): the warps take
+// the partitions round robin (lane l owns dims [D/32 * l, D/32 * (l+1))),
+// two partitions in flight per warp, then merge through shared memory.
+constexpr int kReduceWarps = 8;
+
+template <int V>
+__device__ __forceinline__ void load_floats(const float* p, float (&x)[V]) {
+    if constexpr (V == 4) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w;
+    } else {
+        const float2 a = __ldg(reinterpret_cast<const float2*>(p));
+        x[0] = a.x, x[1] = a.y;
+    }
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(D) lse_reduce_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kReduceWarps * 32)
+    lse_reduce_kernel(const __grid_constant__ ReduceParams p) {
+    constexpr int V = D / 32;                       // floats per lane (4 or 2)
+    __shared__ float red_o[kReduceWarps][D];
+    __shared__ float red_l[kReduceWarps];
+    __shared__ float red_m[kReduceWarps];
+    grid_dependency_wait();
+    allow_dependent_launch();
     const int h = blockIdx.x;
     const int b = blockIdx.y;
-    const int d = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int L = p.context_lens[b];
     if (L < 0 || L > p.max_context) {
-        if (d == 0 && h == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+        if (tid == 0 && h == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
         L = L < 0 ? 0 : p.max_context;
     }
     int S = (L + p.partition_tokens - 1) / p.partition_tokens;
     S = min(S, p.max_parts);
     T* out = reinterpret_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + h) * D;
     if (S <= 0) {
-        out[d] = from_float<T>(0.f);
+        for (int d = tid; d < D; d += blockDim.x) out[d] = from_float<T>(0.f);
         return;
     }
     const size_t base = ((size_t)b * p.num_q_heads + h) * p.max_parts;
     const float* ml = p.max_logits + base;
     const float* es = p.exp_sums + base;
-    const float* o = p.tmp_out + base * D + d;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(ml + s));
-    float num = 0.f, den = 0.f;
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {
+    const float* o = p.tmp_out + base * D + lane * V;
+
+    // M = max_s m_s
+    float m = -INFINITY;
+    for (int s = tid; s < S; s += blockDim.x) m = fmaxf(m, __ldg(ml + s));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) red_m[warp] = m;
+    __syncthreads();
+    float M = red_m[0];
+#pragma unroll
+    for (int w = 1; w < kReduceWarps; ++w) M = fmaxf(M, red_m[w]);
+
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    float den = 0.f;
+    int s = warp;
+    for (; s + kReduceWarps < S; s += 2 * kReduceWarps) {
+        const int s2 = s + kReduceWarps;
         const float w0 = __ldg(es + s) * __expf(__ldg(ml + s) - M);
-        const float w1 = __ldg(es + s + 1) * __expf(__ldg(ml + s + 1) - M);
-        const float w2 = __ldg(es + s + 2) * __expf(__ldg(ml + s + 2) - M);
-        const float w3 = __ldg(es + s + 3) * __expf(__ldg(ml + s + 3) - M);
-        num += w0 * __ldg(o + (size_t)s * D) + w1 * __ldg(o + (size_t)(s + 1) * D) +
-               w2 * __ldg(o + (size_t)(s + 2) * D) + w3 * __ldg(o + (size_t)(s + 3) * D);
-        den += (w0 + w1) + (w2 + w3);
+        const float w1 = __ldg(es + s2) * __expf(__ldg(ml + s2) - M);
+        float x0[V], x1[V];
+        load_floats<V>(o + (size_t)s * D, x0);
+        load_floats<V>(o + (size_t)s2 * D, x1);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += w0 * x0[i] + w1 * x1[i];
+        den += w0 + w1;
     }
-    for (; s < S; ++s) {
-        const float w = __ldg(es + s) * __expf(__ldg(ml + s) - M);
-        num += w * __ldg(o + (size_t)s * D);
-        den += w;
+    if (s < S) {
+        const float w0 = __ldg(es + s) * __expf(__ldg(ml + s) - M);
+        float x0[V];
+        load_floats<V>(o + (size_t)s * D, x0);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += w0 * x0[i];
+        den += w0;
     }
-    out[d] = from_float<T>(num / den);
+#pragma unroll
+    for (int i = 0; i < V; ++i) red_o[warp][lane * V + i] = acc[i];
+    if (lane == 0) red_l[warp] = den;
+    __syncthreads();
+    for (int d = tid; d < D; d += blockDim.x) {
+        float num = 0.f, dd = 0.f;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) {
+            num += red_o[w][d];
+            dd += red_l[w];
+        }
+        out[d] = from_float<T>(num / dd);
+    }
 }
 
 cudaError_t launch_reduce(int dtype, int head_dim, const ReduceParams& p, int num_seqs,
                           cudaStream_t stream) {
     dim3 grid(p.num_q_heads, num_seqs);
+    const dim3 threads(kReduceWarps * 32);
     if (dtype == PA_BF16) {
         if (head_dim == 64)
-            lse_reduce_kernel<__nv_bfloat16, 64><<<grid, 64, 0, stream>>>(p);
-        else
-            lse_reduce_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(p);
-    } else {
-        if (head_dim == 64)
-            lse_reduce_kernel<__half, 64><<<grid, 64, 0, stream>>>(p);
-        else
-            lse_reduce_kernel<__half, 128><<<grid, 128, 0, stream>>>(p);
+            return launch_with_pdl(lse_reduce_kernel<__nv_bfloat16, 64>, grid, threads, 0, stream, p);
+        return launch_with_pdl(lse_reduce_kernel<__nv_bfloat16, 128>, grid, threads, 0, stream, p);
     }
-    return cudaGetLastError();
+    if (head_dim == 64)
+        return launch_with_pdl(lse_reduce_kernel<__half, 64>, grid, threads, 0, stream, p);
+    return launch_with_pdl(lse_reduce_kernel<__half, 128>, grid, threads, 0, stream, p);
 }
 
 }  // namespace pa

@@ -50,7 +50,7 @@ struct DecodeLayout {
 };
 
 template <typename T, int D, bool kSplit>
-__global__ void __launch_bounds__(kDecodeThreads, 3)
+__global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ DecodeParams p) {
@@ -70,6 +70,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 3)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = p.group;
+
+    grid_dependency_wait();          // inputs may come from the previous kernel
+    allow_dependent_launch();
 
     // Context length, bounded so the table row is never overrun.
     const int max_ctx = p.max_blocks_per_seq * p.block_size;
@@ -392,13 +395,16 @@ cudaError_t launch_decode_t(bool split, const CUtensorMap& tmk, const CUtensorMa
         e = cudaFuncSetAttribute(paged_decode_kernel<T, D, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        paged_decode_kernel<T, D, true><<<grid, kDecodeThreads, smem, stream>>>(tmk, tmv, p);
+        e = launch_with_pdl(paged_decode_kernel<T, D, true>, grid, dim3(kDecodeThreads), smem,
+                            stream, tmk, tmv, p);
     } else {
         e = cudaFuncSetAttribute(paged_decode_kernel<T, D, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        paged_decode_kernel<T, D, false><<<grid, kDecodeThreads, smem, stream>>>(tmk, tmv, p);
+        e = launch_with_pdl(paged_decode_kernel<T, D, false>, grid, dim3(kDecodeThreads), smem,
+                            stream, tmk, tmv, p);
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

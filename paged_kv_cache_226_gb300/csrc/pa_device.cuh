@@ -29,6 +29,41 @@ __device__ __forceinline__ void flag_error(int* err, int bits) {
     if (err != nullptr) atomicOr(err, bits);
 }
 
+// ---- programmatic dependent launch ---------------------------------------
+//
+// Kernels of this library are launched with programmatic stream
+// serialisation: a kernel may start while its predecessor in the stream is
+// still running, waits in grid_dependency_wait() until that predecessor has
+// finished and its writes are visible, and lets its own successor start
+// early with allow_dependent_launch().  Every kernel waits before it reads
+// any input, so the stream order of results is unchanged; what overlaps is
+// the launch and CTA set-up latency.
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with the programmatic-stream-serialisation attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_with_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---- mbarrier ------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

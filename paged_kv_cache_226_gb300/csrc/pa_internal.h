@@ -13,7 +13,14 @@ constexpr int kTileTokens = 16;      // tokens per pipeline tile (one box row co
 constexpr int kBoxElems = 64;        // innermost box extent: 64 x 2 B = one 128 B swizzle row
 constexpr int kConsumerWarps = 4;    // warps that compute; one more warp issues TMA
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 8;           // tiles in flight per CTA
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 8
+#endif
+#ifndef PA_DECODE_MIN_CTAS_PER_SM
+#define PA_DECODE_MIN_CTAS_PER_SM 3
+#endif
+constexpr int kStages = PA_DECODE_STAGES;   // tiles in flight per CTA
+constexpr int kMinCtasPerSm = PA_DECODE_MIN_CTAS_PER_SM;
 constexpr int kMaxGroup = 8;         // query heads per KV head served by one CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

@@ -20,7 +20,8 @@ Allocator (youngju.dev "vLLM inference optimization" post, section
 Random physical placement: the initial free list is a seeded permutation of
 the pool, so consecutive logical blocks land anywhere in the pool (the
 techfeed summary of ngrok's "Serving models at scale with vLLM": blocks may be
-scattered anywhere in GPU memory, the block table records where).
+scattered anywhere in GPU memory, the block table records where).  The
+parameter ``placement="sequential"`` hands blocks out in pool order instead.
 
 A slot number is ``physical_block * block_size + offset``.  The token written
 in a decode step is the last one of its sequence: ``context_lens[b]`` counts
@@ -310,6 +311,8 @@ def build_workload(name: Optional[str] = None, seed: Optional[int] = None,
     if nb < need:
         raise ValueError(f"pool of {nb} blocks cannot hold {need}")
     perm = rng.permutation(nb)
+    if p.get("placement", "random") == "sequential":
+        perm = np.arange(nb)[::-1]          # pops 0, 1, 2, ...: blocks in pool order
     pool = BlockPool(nb, bs, order=perm)
     alloc = PagedKVAllocator(pool)
     shared = [pool.allocate() for _ in range(prefix_blocks)]
