@@ -106,7 +106,9 @@ def step_bytes(w: pin.Workload, mode: str, partition: int):
     parts = sum(-(-int(L) // partition) for L in w.context_lens)
     split_w = parts * hq * (d + 2) * 4                  # tmp_out + max_logits + exp_sums
     kernels = {"reshape_and_cache": new_tok + write_tok + w.num_tokens * 8}
-    if mode == "split":
+    if mode == "fused":
+        kernels = {"paged_decode_step": kv + q + out + new_tok + write_tok + w.num_tokens * 8}
+    elif mode == "split":
         kernels["paged_decode_split"] = kv + q + split_w
         kernels["lse_reduce"] = split_w + out
     else:
@@ -310,9 +312,9 @@ def bench_ours(args):
 
     w = make_workload(args, rank)
     max_len = int(w.context_lens.max())
-    mode = args.mode if args.mode != "auto" else lib.choose_mode(
-        w.num_seqs, w.num_kv_heads, max_len, args.partition)
-    partition = args.partition
+    mode = args.mode if args.mode != "auto" else "fused"
+    partition = args.partition or lib.choose_partition(w.num_seqs, w.num_kv_heads, max_len,
+                                                       w.block_size, dev)
     S = lib.num_partitions(max_len, partition)
 
     d = {k: v.to(dev) for k, v in dict(
@@ -413,7 +415,8 @@ def bench_ours(args):
         return 0
 
     hbm, peak_src = peaks()
-    dom = "paged_decode_split" if mode == "split" else "paged_decode"
+    dom = {"split": "paged_decode_split", "single": "paged_decode",
+           "fused": "paged_decode_step"}[mode]
     dom_ms = sum(k2_ms) / len(k2_ms)
     dom_bytes = nb["kernels"][dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -431,12 +434,13 @@ def bench_ours(args):
         "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
         "config": {"workload": f"{w.name}: {pin.DESCRIPTIONS[w.name]}"
                                + (f" with {args.params}" if args.params else ""), "mode": mode,
-                   "partition_tokens": partition if mode == "split" else None,
+                   "partition_tokens": partition if mode != "single" else None,
                    "l2": "flushed before every step (256 MiB write, then 256 MiB read of another "
                          "buffer; outside the step's events)",
                    "kv_bytes": w.kv_bytes_logical(), "kv_bytes_unique": w.kv_bytes_unique(),
                    "bytes_per_step": nb["layer_step"], "seqs_per_gpu": w.num_seqs},
-        "kernels_us": {"reshape_and_cache": round(1e3 * sum(k1_ms) / len(k1_ms), 2),
+        "kernels_us": {**({} if mode == "fused" else
+                          {"reshape_and_cache": round(1e3 * sum(k1_ms) / len(k1_ms), 2)}),
                        dom: round(1e3 * dom_ms, 2),
                        "note": f"event-bracketed, serialised, over {n_attr} more steps; the "
                                f"same step serialised takes {1e3 * serial_ms:.2f} us"},
@@ -447,7 +451,7 @@ def bench_ours(args):
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "traffic": profiled_traffic(args.config, dom)},
         "clocks": clk.summary(t_epoch0, t_epoch1),
-        "gpu_launches": 3 * args.steps if mode == "split" else 2 * args.steps,
+        "gpu_launches": {"split": 3, "single": 2, "fused": 1}[mode] * args.steps,
         "device_errors": errs,
         "wall_s_timed": round(t_wall, 4),
         "e2e": e2e,
@@ -468,8 +472,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama8b", choices=sorted(pin.CONFIGS))
-    ap.add_argument("--mode", default="auto", choices=["auto", "single", "split"])
-    ap.add_argument("--partition", type=int, default=lib.DEFAULT_PARTITION)
+    ap.add_argument("--mode", default="auto", choices=["auto", "single", "split", "fused"])
+    ap.add_argument("--partition", type=int, default=0,
+                    help="tokens per partition (0: chosen from the batch shape)")
     ap.add_argument("--params", default="", help="JSON overrides of the workload parameters")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

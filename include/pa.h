@@ -157,6 +157,30 @@ int pa_reduce(const float* tmp_out, const float* max_logits, const float* exp_su
               int32_t max_num_partitions, void* out, const pa_shape* shp, void* stream);
 
 /*
+ * pa_copy_blocks: copy whole physical blocks between two block pools.  For
+ * each pair p < num_pairs of block_mapping (int64 [num_pairs][2], device):
+ *   src = block_mapping[2p], dst = block_mapping[2p+1],
+ *   k_dst[dst][:][:][:] = k_src[src][:][:][:], v_dst likewise (bit copy).
+ * Copy-on-write: before a request writes into a block it shares with others
+ * (parallel sampling, beam search, a shared prompt), it gets a private copy
+ * (tcdigital article, memory sharing for parallel sampling; youngju.dev post,
+ * Copy-on-Write prefix sharing) -- src and dst pools are the same pool.
+ * Swap: a preempted request's blocks move to CPU memory and back (tcdigital
+ * article, --swap-space; ta-paperlens scheduler, preemption) -- one pool is
+ * pinned host memory reachable from the device (cudaHostAlloc / registered
+ * memory under unified addressing), passed by its device-visible address.
+ * Both pools are laid out [num_blocks][block_size][num_kv_heads][head_dim]
+ * with shp's block_size, num_kv_heads, head_dim and dtype (shp->num_blocks is
+ * not used); src_num_blocks / dst_num_blocks bound the ids.  A pair with an
+ * id out of range is skipped and sets PA_DEVERR_BAD_SLOT.  Pairs must not
+ * write the same destination block twice, nor read a block another pair
+ * writes.  num_pairs <= 65535; num_pairs == 0 enqueues nothing.
+ */
+int pa_copy_blocks(const void* k_src, const void* v_src, int64_t src_num_blocks, void* k_dst,
+                   void* v_dst, int64_t dst_num_blocks, const int64_t* block_mapping,
+                   int64_t num_pairs, const pa_shape* shp, void* stream);
+
+/*
  * Size of the device buffer behind pa_decode_static_workspace: 32 MiB,
  * held on every GPU that loads the library until the process exits.
  */
@@ -197,6 +221,40 @@ int pa_decode_static_workspace(const void* q, const void* k_cache, const void* v
                                float scale, int32_t partition_size,
                                int32_t max_num_partitions, void* out, const pa_shape* shp,
                                void* stream);
+
+/*
+ * pa_decode_step: one decode layer-step in a single launch -- the cache write
+ * of each sequence's new token followed by split decode attention and the
+ * log-sum-exp merge.  Same results as
+ *   pa_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, num_seqs, ...);
+ *   pa_decode_split(...); pa_reduce(...);
+ * for the decode step the pages describe (youngju.dev post,
+ * PagedAttentionManager.append_token, then the table-walking attention of
+ * the ta-paperlens page): token b of k, v ([num_seqs][Hkv][D]) is sequence
+ * b's newest token, position L_b - 1, and slot_mapping[b] must be that
+ * position's slot, block_tables[b][(L_b-1)/bs]*bs + (L_b-1)%bs, or negative
+ * (no new token for b: nothing written).  Any other slot is not written and
+ * sets PA_DEVERR_BAD_SLOT.  The CTA of each sequence's last partition writes
+ * the new token into the cache and uses it directly; the last CTA of each
+ * (sequence, KV head) to finish merges its partitions, so no second launch
+ * is needed.
+ *
+ * Workspace: tmp_out, max_logits, exp_sums as for pa_decode_split, plus
+ * counters, int32 [num_seqs][num_kv_heads], which must be zero on entry and
+ * are zero again when the step has run (set them to zero once after
+ * allocation; after a PA_DEVERR_WAIT_TIMEOUT, zero them again).  The merge
+ * stages its weights in shared memory: (Hq/Hkv) * (max_num_partitions + 1)
+ * must not exceed 2096 at head_dim 128 or 1072 at head_dim 64, else
+ * PA_ERR_UNSUPPORTED.  out [B][Hq][D] receives the
+ * attention output.  All pointers device; k, v, out, tmp_out, max_logits,
+ * exp_sums 16-byte aligned; errors as pa_decode_split.
+ */
+int pa_decode_step(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                   void* k_cache, void* v_cache, const int32_t* block_tables,
+                   const int32_t* context_lens, float scale, int32_t partition_size,
+                   int32_t max_num_partitions, float* tmp_out, float* max_logits,
+                   float* exp_sums, int32_t* counters, void* out, const pa_shape* shp,
+                   void* stream);
 
 /* Static description of a status code. */
 const char* pa_status_string(int status);

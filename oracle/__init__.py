@@ -69,6 +69,8 @@ def _load():
             lib.oracle_contiguous_decode.restype = i32
             lib.oracle_contiguous_decode.argtypes = [P, P, P, P, P, f64, i32, i32, i32, i32,
                                                      i32, P]
+            lib.oracle_copy_blocks.restype = i64
+            lib.oracle_copy_blocks.argtypes = [P, P, i64, P, P, i64, P, i64, i32, i32, i32]
             lib.oracle_max_threads.restype = i32
             lib.oracle_max_threads.argtypes = []
             lib.oracle_set_threads.restype = None
@@ -171,6 +173,20 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, block_size: int):
     bad = _load().oracle_reshape_and_cache(_ptr(k), _ptr(v), _ptr(sm), _ptr(kc), _ptr(vc),
                                            T, hkv, d, bs, nb)
     return kc, vc, int(bad)
+
+
+def copy_blocks(k_src, v_src, k_dst, v_dst, mapping):
+    """Return (k_dst', v_dst', n_skipped): copies of the destination pools with
+    the mapped blocks copied in.  Pools [NB][bs][Hkv][D] bits; mapping int64
+    [P][2] of (src, dst)."""
+    ks, vs = _u16(k_src), _u16(v_src)
+    kd, vd = _u16(k_dst).copy(), _u16(v_dst).copy()
+    mp = np.ascontiguousarray(mapping, dtype=np.int64).reshape(-1, 2)
+    _, bs, hkv, d = ks.shape
+    assert kd.shape[1:] == ks.shape[1:] and vs.shape == ks.shape and vd.shape == kd.shape
+    bad = _load().oracle_copy_blocks(_ptr(ks), _ptr(vs), ks.shape[0], _ptr(kd), _ptr(vd),
+                                     kd.shape[0], _ptr(mp), mp.shape[0], bs, hkv, d)
+    return kd, vd, int(bad)
 
 
 def _decode_args(q, k_cache, v_cache, block_tables, context_lens):

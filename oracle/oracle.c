@@ -113,6 +113,32 @@ int64_t oracle_reshape_and_cache(const uint16_t* k, const uint16_t* v,
     return bad;
 }
 
+/* ---- whole-block copies: copy-on-write and swap ------------------------ */
+
+/*
+ * For each pair p: dst pool block mapping[2p+1] receives a bit copy of src
+ * pool block mapping[2p], for K and V (a block is block_size * num_kv_heads
+ * * head_dim elements).  Copy-on-write gives a request its own copy of a
+ * shared block before it writes there (tcdigital article, memory sharing for
+ * parallel sampling; youngju.dev post, Copy-on-Write); swapping moves blocks
+ * between GPU and CPU pools (tcdigital article, --swap-space).  Pairs with
+ * an id outside either pool are skipped and counted; the count is returned.
+ */
+int64_t oracle_copy_blocks(const uint16_t* k_src, const uint16_t* v_src, int64_t src_blocks,
+                           uint16_t* k_dst, uint16_t* v_dst, int64_t dst_blocks,
+                           const int64_t* mapping, int64_t num_pairs, int block_size,
+                           int num_kv_heads, int head_dim) {
+    int64_t elems = (int64_t)block_size * num_kv_heads * head_dim;
+    int64_t bad = 0;
+    for (int64_t p = 0; p < num_pairs; ++p) {
+        int64_t s = mapping[2 * p], d = mapping[2 * p + 1];
+        if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) { ++bad; continue; }
+        memcpy(k_dst + d * elems, k_src + s * elems, (size_t)elems * sizeof(uint16_t));
+        memcpy(v_dst + d * elems, v_src + s * elems, (size_t)elems * sizeof(uint16_t));
+    }
+    return bad;
+}
+
 /* ---- attention over one span of one sequence -------------------------- */
 
 /*

@@ -137,6 +137,7 @@ pa::DecodeParams make_params(const void* q, const int32_t* block_tables,
     p.max_blocks_per_seq = shp->max_blocks_per_seq;
     p.block_size = shp->block_size;
     p.num_blocks = shp->num_blocks;
+    p.num_kv_heads = shp->num_kv_heads;
     return p;
 }
 
@@ -214,7 +215,7 @@ int pa_decode(const void* q, const void* k_cache, const void* v_cache,
     pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err);
     p.out = out;
     dim3 grid(1, shp->num_kv_heads, shp->num_seqs);
-    e = pa::launch_decode(shp->dtype, shp->head_dim, false, tmk, tmv, p, grid,
+    e = pa::launch_decode(shp->dtype, shp->head_dim, pa::kModeSingle, tmk, tmv, p, grid,
                           static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
@@ -254,8 +255,77 @@ int pa_decode_split(const void* q, const void* k_cache, const void* v_cache,
     p.partition_tokens = partition_size;
     p.max_parts = max_num_partitions;
     dim3 grid(max_num_partitions, shp->num_kv_heads, shp->num_seqs);
-    e = pa::launch_decode(shp->dtype, shp->head_dim, true, tmk, tmv, p, grid,
+    e = pa::launch_decode(shp->dtype, shp->head_dim, pa::kModeSplit, tmk, tmv, p, grid,
                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_decode_step(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                   void* k_cache, void* v_cache, const int32_t* block_tables,
+                   const int32_t* context_lens, float scale, int32_t partition_size,
+                   int32_t max_num_partitions, float* tmp_out, float* max_logits,
+                   float* exp_sums, int32_t* counters, void* out, const pa_shape* shp,
+                   void* stream) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
+    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !out || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    if (!tmp_out || !max_logits || !exp_sums || !counters) return PA_ERR_WORKSPACE;
+    if (!aligned16(tmp_out) || !aligned16(max_logits) || !aligned16(exp_sums) ||
+        (reinterpret_cast<uintptr_t>(counters) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int G = shp->num_q_heads / shp->num_kv_heads;
+    if ((int64_t)G * max_num_partitions + G > pa::decode_merge_floats(shp->head_dim))
+        return PA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp)) != PA_OK) return st;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err);
+    p.out = out;
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.partition_tokens = partition_size;
+    p.max_parts = max_num_partitions;
+    p.k_new = k;
+    p.v_new = v;
+    p.slot_mapping = slot_mapping;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.counters = counters;
+    dim3 grid(max_num_partitions, shp->num_kv_heads, shp->num_seqs);
+    e = pa::launch_decode(shp->dtype, shp->head_dim, pa::kModeStep, tmk, tmv, p, grid,
+                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_copy_blocks(const void* k_src, const void* v_src, int64_t src_num_blocks, void* k_dst,
+                   void* v_dst, int64_t dst_num_blocks, const int64_t* block_mapping,
+                   int64_t num_pairs, const pa_shape* shp, void* stream) {
+    int st = check_shape(shp, false);
+    if (st != PA_OK) return st;
+    if (num_pairs < 0 || num_pairs > 65535 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_src || !v_src || !k_dst || !v_dst || !block_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(k_dst) || !aligned16(v_dst) ||
+        (reinterpret_cast<uintptr_t>(block_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int64_t block_bytes =
+        (int64_t)shp->block_size * shp->num_kv_heads * shp->head_dim * 2;
+    e = pa::launch_copy_blocks(k_src, v_src, src_num_blocks, k_dst, v_dst, dst_num_blocks,
+                               block_mapping, num_pairs, block_bytes, err,
+                               static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

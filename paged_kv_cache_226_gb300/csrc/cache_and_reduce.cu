@@ -4,16 +4,16 @@
 
 namespace pa {
 
-cudaError_t launch_decode_f16(int, bool, const CUtensorMap&, const CUtensorMap&,
+cudaError_t launch_decode_f16(int, int, const CUtensorMap&, const CUtensorMap&,
                               const DecodeParams&, dim3, cudaStream_t);
-cudaError_t launch_decode_bf16(int, bool, const CUtensorMap&, const CUtensorMap&,
+cudaError_t launch_decode_bf16(int, int, const CUtensorMap&, const CUtensorMap&,
                                const DecodeParams&, dim3, cudaStream_t);
 
-cudaError_t launch_decode(int dtype, int head_dim, bool split, const CUtensorMap& tmk,
+cudaError_t launch_decode(int dtype, int head_dim, int mode, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
                           cudaStream_t stream) {
-    if (dtype == PA_BF16) return launch_decode_bf16(head_dim, split, tmk, tmv, p, grid, stream);
-    return launch_decode_f16(head_dim, split, tmk, tmv, p, grid, stream);
+    if (dtype == PA_BF16) return launch_decode_bf16(head_dim, mode, tmk, tmv, p, grid, stream);
+    return launch_decode_f16(head_dim, mode, tmk, tmv, p, grid, stream);
 }
 
 // ---------------------------------------------------------------------------

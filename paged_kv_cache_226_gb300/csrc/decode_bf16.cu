@@ -3,11 +3,11 @@
 
 namespace pa {
 
-cudaError_t launch_decode_bf16(int head_dim, bool split, const CUtensorMap& tmk,
+cudaError_t launch_decode_bf16(int head_dim, int mode, const CUtensorMap& tmk,
                                const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
                                cudaStream_t stream) {
-    if (head_dim == 64) return launch_decode_t<__nv_bfloat16, 64>(split, tmk, tmv, p, grid, stream);
-    return launch_decode_t<__nv_bfloat16, 128>(split, tmk, tmv, p, grid, stream);
+    if (head_dim == 64) return launch_decode_t<__nv_bfloat16, 64>(mode, tmk, tmv, p, grid, stream);
+    return launch_decode_t<__nv_bfloat16, 128>(mode, tmk, tmv, p, grid, stream);
 }
 
 }  // namespace pa

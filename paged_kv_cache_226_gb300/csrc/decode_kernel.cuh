@@ -8,8 +8,8 @@
 // Data movement: a producer warp reads the block table and issues one TMA
 // box per 16-token half-row tile ([16 tokens][64 dims] of one KV head, 128 B
 // rows, 128 B swizzle) into an 8-stage shared-memory ring guarded by
-// mbarriers; a block of 32 tokens is two tiles.  Four consumer warps take the
-// tiles round robin.
+// mbarriers; a block of 32 tokens is two tiles.  The consumer warps (two by
+// default, with a 4-stage ring and six CTAs per SM) take the tiles round robin.
 //
 // Math per tile and warp (the G <= 8 query heads of the group are the N = 8
 // columns of two m16n8k16 tile products; columns >= G are zero):
@@ -49,7 +49,7 @@ struct DecodeLayout {
     static constexpr int kDynamicSmem = kBodyBytes + 1024;         // + alignment slack
 };
 
-template <typename T, int D, bool kSplit>
+template <typename T, int D, int kMode>
 __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
@@ -59,8 +59,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     constexpr int kKSteps = D / 16;     // 16-dim slices of D
     constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
 
+    constexpr bool kPartitioned = kMode != kModeSingle;
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ int merge_here;          // fused step: this CTA merges the partitions
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -81,9 +83,18 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
         if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
         L = L < 0 ? 0 : max_ctx;
     }
-    int t_begin = 0, t_end = L;
-    if (kSplit) {
+    int t_begin = 0, t_end = L, parts = 1;
+    if (kPartitioned) {
+        parts = min((L + p.partition_tokens - 1) / p.partition_tokens, p.max_parts);
         t_begin = blockIdx.x * p.partition_tokens;
+        if (kMode == kModeStep && L == 0 && blockIdx.x == 0) {
+            // Empty context: zero output; a new token cannot belong to it.
+            T* out = reinterpret_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)g * G) * D;
+            for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = from_float<T>(0.f);
+            if (threadIdx.x == 0 && g == 0 && p.slot_mapping[b] >= 0)
+                flag_error(p.err, PA_DEVERR_BAD_SLOT);
+            return;
+        }
         if (t_begin >= L) return;                       // partition past the end
         t_end = min(t_begin + p.partition_tokens, L);
     } else if (L == 0) {
@@ -194,6 +205,27 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     const int v_tok = (lane >> 4) * 8 + (lane & 7);
     const int v_hi = (lane >> 3) & 1;
 
+    // Fused step: the CTA of the last partition owns the sequence's new token
+    // (position L - 1).  It checks that slot_mapping[b] is that position's
+    // slot, writes the token's K/V for this KV head into the cache, and puts
+    // them into the staged tile in place of what the TMA read there.
+    int64_t new_slot = -1;
+    int new_tile = -1;                      // CTA-local tile index, -1: not attended here
+    if (kMode == kModeStep && blockIdx.x == parts - 1) {
+        const int64_t slot = p.slot_mapping[b];
+        if (slot >= 0) {
+            const int pos = L - 1;
+            const int64_t blk = p.block_tables[(size_t)b * p.max_blocks_per_seq + pos / p.block_size];
+            const int64_t want = blk * p.block_size + pos % p.block_size;
+            if (slot == want && blk >= 0 && blk < p.num_blocks) {
+                new_slot = slot;
+                if (pos < t_end) new_tile = pos / kTileTokens - tile_begin;
+            } else if (warp == 0 && lane == 0) {
+                flag_error(p.err, PA_DEVERR_BAD_SLOT);
+            }
+        }
+    }
+
     for (int it = warp; it < n_tiles; it += kConsumerWarps) {
         const int st = it % kStages;
         bool ok = mbar_wait(&full_bar[st], (it / kStages) & 1);
@@ -205,6 +237,25 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
         uint8_t* vtile = ktile + Lay::kTileBytes;
         const uint32_t kbase = smem_u32(ktile);
         const uint32_t vbase = smem_u32(vtile);
+
+        if (kMode == kModeStep && it == new_tile) {
+            // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V
+            const int r = (L - 1) % kTileTokens;
+            const int c = lane & 15;
+            if (c < D / 8) {
+                const bool is_k = lane < 16;
+                const size_t row = ((size_t)b * p.num_kv_heads + g) * D;
+                const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                                            reinterpret_cast<const T*>(is_k ? p.k_new : p.v_new) + row) + c);
+                uint8_t* tile = is_k ? ktile : vtile;
+                *reinterpret_cast<uint4*>(tile + (c >> 3) * Lay::kBoxBytes + r * 128 +
+                                          (((c & 7) ^ (r & 7)) << 4)) = val;
+                T* cache = reinterpret_cast<T*>(is_k ? p.k_cache : p.v_cache);
+                reinterpret_cast<uint4*>(cache + ((size_t)new_slot * p.num_kv_heads + g) * D)[c] = val;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
 
         // S^T for the 16 tokens of the tile
         float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -303,6 +354,18 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
         if (lane == 0) mbar_arrive(&empty_bar[st]);
     }
 
+    if (kMode == kModeStep && new_slot >= 0 && new_tile < 0 && warp == 0) {
+        const int c = lane & 15;
+        if (c < D / 8) {
+            const bool is_k = lane < 16;
+            const size_t row = ((size_t)b * p.num_kv_heads + g) * D;
+            const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                                        reinterpret_cast<const T*>(is_k ? p.k_new : p.v_new) + row) + c);
+            T* cache = reinterpret_cast<T*>(is_k ? p.k_cache : p.v_cache);
+            reinterpret_cast<uint4*>(cache + ((size_t)new_slot * p.num_kv_heads + g) * D)[c] = val;
+        }
+    }
+
     // row sums across the 8 lanes that share a head pair
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -369,7 +432,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
         }
         const float inv = 1.f / den;
         const size_t qh = (size_t)b * p.num_q_heads + (size_t)g * G + h;
-        if (kSplit) {
+        if (kMode == kModeSplit || (kMode == kModeStep && parts > 1)) {
             const size_t idx = qh * p.max_parts + blockIdx.x;
             *reinterpret_cast<float4*>(p.tmp_out + idx * D + d) =
                 make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
@@ -384,28 +447,100 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
             *reinterpret_cast<uint2*>(out) = make_uint2(lo, hi);
         }
     }
+
+    if (kMode == kModeStep && parts > 1) {
+        // The last CTA of the (sequence, KV head) to finish merges all
+        // partitions: M = max m_s, w_s = l_s e^(m_s - M), out = sum w_s o_s / sum w_s.
+        __threadfence();                                   // partials before the count
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        int* counter = p.counters + (size_t)b * p.num_kv_heads + g;
+        if (tid == 0) merge_here = (atomicAdd(counter, 1) == parts - 1);
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        if (!merge_here) return;
+        __threadfence();                                   // other CTAs' partials visible
+        const size_t qh0 = (size_t)b * p.num_q_heads + (size_t)g * G;
+        // weights w[h][s] (natural-log units) into the merge area; one warp per head
+        float* wts = mrg;                                  // [G][parts]
+        float* dens = mrg + G * parts;                     // [G]
+        for (int h = warp; h < G; h += kConsumerWarps) {
+            const float* ml = p.max_logits + (qh0 + h) * p.max_parts;
+            const float* es = p.exp_sums + (qh0 + h) * p.max_parts;
+            float mx = -INFINITY;
+            for (int s2 = lane; s2 < parts; s2 += 32) mx = fmaxf(mx, __ldcg(ml + s2));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float dsum = 0.f;
+            for (int s2 = lane; s2 < parts; s2 += 32) {
+                const float wv = __ldcg(es + s2) * __expf(__ldcg(ml + s2) - mx);
+                wts[h * parts + s2] = wv;
+                dsum += wv;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+            if (lane == 0) dens[h] = dsum;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        for (int item = tid; item < items; item += kConsumerWarps * 32) {
+            const int h = item / (D / 4);
+            const int d = (item - h * (D / 4)) * 4;
+            const float* src = p.tmp_out + (qh0 + h) * p.max_parts * D + d;
+            const float* wh = wts + h * parts;
+            // four partitions in flight per thread
+            float4 acc4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            int s2 = 0;
+            for (; s2 + 4 <= parts; s2 += 4) {
+                float4 x[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    x[j] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(s2 + j) * D));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float wj = wh[s2 + j];
+                    acc4[j].x += wj * x[j].x; acc4[j].y += wj * x[j].y;
+                    acc4[j].z += wj * x[j].z; acc4[j].w += wj * x[j].w;
+                }
+            }
+            for (; s2 < parts; ++s2) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (size_t)s2 * D));
+                const float wj = wh[s2];
+                acc4[0].x += wj * x.x; acc4[0].y += wj * x.y;
+                acc4[0].z += wj * x.z; acc4[0].w += wj * x.w;
+            }
+            const float4 a = make_float4(acc4[0].x + acc4[1].x, acc4[0].y + acc4[1].y,
+                                         acc4[0].z + acc4[1].z, acc4[0].w + acc4[1].w);
+            const float4 c = make_float4(acc4[2].x + acc4[3].x, acc4[2].y + acc4[3].y,
+                                         acc4[2].z + acc4[3].z, acc4[2].w + acc4[3].w);
+            const float inv = 1.f / dens[h];
+            T* out = reinterpret_cast<T*>(p.out) + (qh0 + h) * D + d;
+            const uint32_t lo = M::pack((a.x + c.x) * inv, (a.y + c.y) * inv);
+            const uint32_t hi = M::pack((a.z + c.z) * inv, (a.w + c.w) * inv);
+            *reinterpret_cast<uint2*>(out) = make_uint2(lo, hi);
+        }
+        if (tid == 0) *counter = 0;                        // ready for the next step
+    }
+}
+
+template <typename T, int D, int kMode>
+cudaError_t launch_decode_mode(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                               const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+    const int smem = DecodeLayout<D>::kDynamicSmem;
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, kMode>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = launch_with_pdl(paged_decode_kernel<T, D, kMode>, grid, dim3(kDecodeThreads), smem,
+                        stream, tmk, tmv, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 template <typename T, int D>
-cudaError_t launch_decode_t(bool split, const CUtensorMap& tmk, const CUtensorMap& tmv,
+cudaError_t launch_decode_t(int mode, const CUtensorMap& tmk, const CUtensorMap& tmv,
                             const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-    const int smem = DecodeLayout<D>::kDynamicSmem;
-    cudaError_t e;
-    if (split) {
-        e = cudaFuncSetAttribute(paged_decode_kernel<T, D, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        e = launch_with_pdl(paged_decode_kernel<T, D, true>, grid, dim3(kDecodeThreads), smem,
-                            stream, tmk, tmv, p);
-    } else {
-        e = cudaFuncSetAttribute(paged_decode_kernel<T, D, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        e = launch_with_pdl(paged_decode_kernel<T, D, false>, grid, dim3(kDecodeThreads), smem,
-                            stream, tmk, tmv, p);
-    }
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    if (mode == kModeSplit) return launch_decode_mode<T, D, kModeSplit>(tmk, tmv, p, grid, stream);
+    if (mode == kModeStep) return launch_decode_mode<T, D, kModeStep>(tmk, tmv, p, grid, stream);
+    return launch_decode_mode<T, D, kModeSingle>(tmk, tmv, p, grid, stream);
 }
 
 }  // namespace pa

@@ -11,16 +11,24 @@ namespace pa {
 
 constexpr int kTileTokens = 16;      // tokens per pipeline tile (one box row count)
 constexpr int kBoxElems = 64;        // innermost box extent: 64 x 2 B = one 128 B swizzle row
-constexpr int kConsumerWarps = 4;    // warps that compute; one more warp issues TMA
+#ifndef PA_DECODE_CONSUMER_WARPS
+#define PA_DECODE_CONSUMER_WARPS 2
+#endif
+constexpr int kConsumerWarps = PA_DECODE_CONSUMER_WARPS;  // warps that compute; +1 issues TMA
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 #ifndef PA_DECODE_STAGES
-#define PA_DECODE_STAGES 8
+#define PA_DECODE_STAGES 4
 #endif
 #ifndef PA_DECODE_MIN_CTAS_PER_SM
-#define PA_DECODE_MIN_CTAS_PER_SM 3
+#define PA_DECODE_MIN_CTAS_PER_SM 6
 #endif
 constexpr int kStages = PA_DECODE_STAGES;   // tiles in flight per CTA
 constexpr int kMinCtasPerSm = PA_DECODE_MIN_CTAS_PER_SM;
+// Consumer warp w takes tiles w, w + W, w + 2W, ... and tile i sits in stage
+// i % kStages.  With kStages a multiple of W every stage belongs to exactly
+// one warp, which waits on its phases in order; otherwise two warps would
+// share a stage and a parity wait could match a phase two laps old.
+static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
 constexpr int kMaxGroup = 8;         // query heads per KV head served by one CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -42,7 +50,20 @@ struct DecodeParams {
     int64_t num_blocks;
     int partition_tokens;          // split: partition size; single pass: 0
     int max_parts;                 // split: S
+    // fused layer-step only
+    const void* k_new;             // [B][Hkv][D] new token of each sequence
+    const void* v_new;
+    const int64_t* slot_mapping;   // [B] slot of position L_b - 1 (negative: none)
+    void* k_cache;                 // written at the new token's slot
+    void* v_cache;
+    int* counters;                 // [B][Hkv] arrivals per (sequence, KV head), 0 on entry
+    int num_kv_heads;
 };
+
+// Decode kernel modes.
+constexpr int kModeSingle = 0;   // one CTA per (sequence, KV head), final output
+constexpr int kModeSplit = 1;    // one CTA per partition, partial outputs
+constexpr int kModeStep = 2;     // split + cache write of the new token + in-kernel merge
 
 struct ReduceParams {
     const float* tmp_out;
@@ -58,15 +79,22 @@ struct ReduceParams {
 };
 
 // Kernel launchers (kernels live in their own translation units).
-cudaError_t launch_decode(int dtype, int head_dim, bool split, const CUtensorMap& tmk,
+cudaError_t launch_decode(int dtype, int head_dim, int mode, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
                           cudaStream_t stream);
+// Float capacity of the decode kernel's merge area (bounds G * S in the fused step).
+int decode_merge_floats(int head_dim);
 cudaError_t launch_reduce(int dtype, int head_dim, const ReduceParams& p, int num_seqs,
                           cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int64_t* slots,
                                      void* kc, void* vc, int64_t num_tokens,
                                      int64_t num_slots, int row_bytes, int* err,
                                      cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(const void* k_src, const void* v_src, int64_t src_blocks,
+                               void* k_dst, void* v_dst, int64_t dst_blocks,
+                               const int64_t* mapping, int64_t num_pairs, int64_t block_bytes,
+                               int* err, cudaStream_t stream);
 
 // Sets the value pa_last_cuda_error() reports on this host thread.
 void record_cuda_error(int cuda_error);

@@ -88,6 +88,8 @@ class PagedKVAllocator:
         self.block_size = pool.block_size
         self.page_tables: Dict[int, List[int]] = {}
         self.token_counts: Dict[int, int] = {}
+        self.pending_copies: List[tuple] = []
+        self.swapped: Dict[int, BlockPool] = {}
 
     def add_sequence(self, seq_id: int, shared_prefix: Sequence[int] = (),
                      prefix_tokens: int = 0) -> None:
@@ -109,15 +111,70 @@ class PagedKVAllocator:
             self.token_counts[seq_id] = 0
 
     def append_token(self, seq_id: int) -> int:
-        """Reserve the slot of the request's next token and return it."""
+        """Reserve the slot of the request's next token and return it.
+
+        If the token lands in a block that other requests still share, the
+        request first gets a private copy of that block (copy-on-write); the
+        (source, destination) pair is queued in ``pending_copies`` and must be
+        copied on the device before the token is written."""
         table = self.page_tables[seq_id]
         count = self.token_counts[seq_id]
         slot_in_block = count % self.block_size
         if slot_in_block == 0 and count > 0:
             table.append(self.pool.allocate())
+        elif self.pool.ref_count[table[-1]] > 1:
+            shared = table[-1]
+            private = self.pool.allocate()
+            self.pending_copies.append((shared, private))
+            self.pool.free(shared)
+            table[-1] = private
         last_block = table[-1]
         self.token_counts[seq_id] = count + 1
         return last_block * self.block_size + slot_in_block
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        """The child shares every block of the parent (parallel sampling,
+        beam search): reference counts rise, nothing is copied yet."""
+        if child_id in self.page_tables:
+            raise ValueError(f"sequence {child_id} exists")
+        for p in self.page_tables[parent_id]:
+            self.pool.share(p)
+        self.page_tables[child_id] = list(self.page_tables[parent_id])
+        self.token_counts[child_id] = self.token_counts[parent_id]
+
+    def take_copies(self) -> List[tuple]:
+        """Copy-on-write pairs queued since the last call."""
+        out, self.pending_copies = self.pending_copies, []
+        return out
+
+    def swap_out(self, seq_id: int, host_pool: "BlockPool") -> List[tuple]:
+        """Move a request's blocks to ``host_pool``: returns (device block,
+        host block) pairs to copy; the device blocks return to the free list.
+        Blocks still shared with other requests cannot be swapped out."""
+        table = self.page_tables[seq_id]
+        if any(self.pool.ref_count[p] > 1 for p in table):
+            raise ValueError("cannot swap out shared blocks")
+        pairs = []
+        for i, p in enumerate(table):
+            h = host_pool.allocate()
+            pairs.append((p, h))
+            self.pool.free(p)
+            table[i] = h
+        self.swapped[seq_id] = host_pool
+        return pairs
+
+    def swap_in(self, seq_id: int) -> List[tuple]:
+        """Bring a swapped-out request back: returns (host block, device
+        block) pairs to copy; the host blocks return to their free list."""
+        host_pool = self.swapped.pop(seq_id)
+        table = self.page_tables[seq_id]
+        pairs = []
+        for i, h in enumerate(table):
+            p = self.pool.allocate()
+            pairs.append((h, p))
+            host_pool.free(h)
+            table[i] = p
+        return pairs
 
     def extend(self, seq_id: int, n: int) -> None:
         """Same effect as ``n`` calls of ``append_token`` (slots not returned)."""

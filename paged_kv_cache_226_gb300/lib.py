@@ -65,6 +65,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pa_split_workspace_size.restype = ctypes.c_size_t
         lib.pa_decode_split.argtypes = [V, V, V, V, V, F, I32, I32, V, V, V, S, V]
         lib.pa_reduce.argtypes = [V, V, V, V, I32, I32, V, S, V]
+        lib.pa_copy_blocks.argtypes = [V, V, I64, V, V, I64, V, I64, S, V]
+        lib.pa_copy_blocks.restype = ctypes.c_int
+        lib.pa_decode_step.argtypes = [V, V, V, V, V, V, V, V, F, I32, I32, V, V, V, V, V, S, V]
+        lib.pa_decode_step.restype = ctypes.c_int
         lib.pa_decode_static_workspace.argtypes = [V, V, V, V, V, F, I32, I32, V, S, V]
         lib.pa_decode_static_workspace.restype = ctypes.c_int
         lib.pa_status_string.argtypes = [ctypes.c_int]
@@ -269,6 +273,72 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: floa
     return reduce(tmp, ml, es, context_lens, partition_size, k_cache, block_tables.shape[1], out)
 
 
+def copy_blocks(k_src: torch.Tensor, v_src: torch.Tensor, k_dst: torch.Tensor,
+                v_dst: torch.Tensor, block_mapping: torch.Tensor,
+                device: Optional[torch.device] = None) -> None:
+    """Copy whole blocks ``(src, dst)`` of ``block_mapping`` (int64 [P][2], on
+    the device) from the src pools to the dst pools (pa_copy_blocks): the same
+    pool for copy-on-write, a pinned host pool on one side for swapping."""
+    lib = load()
+    dev = device or block_mapping.device
+    _need(block_mapping, "block_mapping", torch.int64, dev)
+    for t, n in ((k_src, "k_src"), (v_src, "v_src"), (k_dst, "k_dst"), (v_dst, "v_dst")):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous() or t.dtype != k_src.dtype or t.dim() != 4:
+            raise ValueError(f"{n} must be a contiguous 4-D pool of {k_src.dtype}")
+        if t.shape[1:] != k_src.shape[1:]:
+            raise ValueError("pools differ in block shape")
+    if v_src.shape != k_src.shape or v_dst.shape != k_dst.shape:
+        raise ValueError("K and V pools differ in shape")
+    mp = block_mapping.reshape(-1, 2)
+    shp = make_shape(0, k_src.shape[2], k_src, 1)
+    with torch.cuda.device(dev):
+        _check("pa_copy_blocks",
+               lib.pa_copy_blocks(_ptr(k_src), _ptr(v_src), k_src.shape[0], _ptr(k_dst),
+                                  _ptr(v_dst), k_dst.shape[0], _ptr(mp), mp.shape[0],
+                                  ctypes.byref(shp), _stream_handle(dev)))
+
+
+def step_workspace(q: torch.Tensor, num_kv_heads: int, max_num_partitions: int):
+    """(tmp_out, max_logits, exp_sums, counters) for ``decode_step``; the
+    counters start at zero and every step leaves them at zero."""
+    tmp, ml, es = split_workspace(q, max_num_partitions)
+    counters = torch.zeros((q.shape[0], num_kv_heads), dtype=torch.int32, device=q.device)
+    return tmp, ml, es, counters
+
+
+def decode_step(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens,
+                scale: float, max_context_len: int, out: Optional[torch.Tensor] = None,
+                partition_size: int = DEFAULT_PARTITION, workspace=None) -> torch.Tensor:
+    """One fused decode layer-step (pa_decode_step): write each sequence's new
+    token into the cache and attend, merging partitions in the same launch."""
+    lib = load()
+    shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, k_cache.dtype, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    if k_new.shape != (q.shape[0], k_cache.shape[2], k_cache.shape[3]) or \
+            v_new.shape != k_new.shape or slot_mapping.shape != (q.shape[0],):
+        raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim], "
+                         "slot_mapping [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", q.dtype, dev)
+    S = num_partitions(max_context_len, partition_size)
+    if workspace is None:
+        workspace = step_workspace(q, k_cache.shape[2], S)
+    tmp, ml, es, counters = workspace
+    _need(counters, "counters", torch.int32, dev)
+    _check("pa_decode_step",
+           lib.pa_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                              _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                              _ptr(context_lens), float(scale), int(partition_size), int(S),
+                              _ptr(tmp), _ptr(ml), _ptr(es), _ptr(counters), _ptr(out),
+                              ctypes.byref(shp), _stream_handle(dev)))
+    return out
+
+
 STATIC_WORKSPACE_BYTES = 32 << 20
 
 
@@ -295,6 +365,33 @@ def decode_static_workspace(q, k_cache, v_cache, block_tables, context_lens, sca
     return out
 
 
+CTAS_PER_SM = 6          # resident decode CTAs per SM in the shipped build
+
+
+def choose_partition(num_seqs: int, num_kv_heads: int, max_context_len: int,
+                     block_size: int = 16, device=None) -> int:
+    """Partition size for the split / fused paths.
+
+    With at least half as many (sequence, KV head) pairs as resident CTA
+    slots, 512-token partitions already give every slot work and keep the
+    merge short.  Fewer pairs (long contexts, small batches) get longer
+    partitions, about one partition per slot, so the per-partition start-up
+    cost is paid fewer times: round_up(max_len * pairs / slots, 512),
+    clamped to [512, 4096]."""
+    if device is None and torch.cuda.is_available():
+        device = torch.cuda.current_device()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count if device is not None \
+        else 152
+    slots = sms * CTAS_PER_SM
+    pairs = max(1, num_seqs * num_kv_heads)
+    if 2 * pairs >= slots or max_context_len <= 512:
+        p = 512
+    else:
+        p = -(-max_context_len * pairs // slots)
+        p = min(4096, max(512, -(-p // 512) * 512))
+    return max(block_size, p - p % block_size)
+
+
 def choose_mode(num_seqs: int, num_kv_heads: int, max_context_len: int, partition_size: int,
                 device=None) -> str:
     """Single pass when every (sequence, KV head) CTA is short, else split."""
@@ -317,9 +414,10 @@ def read_device_errors(device: Optional[torch.device] = None) -> int:
 class StepPlan:
     """One decode layer-step with its arguments marshalled once.
 
-    Holds the C-ABI argument lists of reshape_and_cache, the decode kernel
-    (single pass, or split + merge) for fixed tensors, so that each launch
-    costs one ctypes call.  The work goes to the caller's current stream at
+    Holds the C-ABI argument lists of the step for fixed tensors, so that
+    each launch costs one ctypes call.  Modes: ``"fused"`` (the default: one
+    pa_decode_step launch), ``"split"`` (reshape_and_cache, decode_split,
+    reduce) and ``"single"`` (reshape_and_cache, decode).  The work goes to the caller's current stream at
     call time, which also makes a step capturable into a CUDA graph
     (``capture_graph``).  The tensors must stay alive and keep their shapes;
     their contents (new tokens, tables, lengths) may change between steps as
@@ -341,9 +439,11 @@ class StepPlan:
         self.out = torch.empty_like(q) if out is None else out
         _need(self.out, "out", q.dtype, dev)
         if mode == "auto":
-            mode = choose_mode(q.shape[0], k_cache.shape[2], max_context_len, partition_size)
-        if mode not in ("single", "split"):
+            mode = "fused"
+        if mode not in ("single", "split", "fused"):
             raise ValueError(f"unknown mode {mode!r}")
+        if mode == "fused" and T != q.shape[0]:
+            raise ValueError("the fused step takes exactly one new token per sequence")
         self.mode = mode
         self.partition_size = int(partition_size)
         self.num_partitions = num_partitions(max_context_len, partition_size)
@@ -356,6 +456,18 @@ class StepPlan:
         if mode == "single":
             self._decode_args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                  _ptr(context_lens), ctypes.c_float(scale), _ptr(self.out), sref)
+        elif mode == "fused":
+            if workspace is None:
+                workspace = step_workspace(q, k_cache.shape[2], self.num_partitions)
+            tmp, ml, es, counters = workspace
+            self.workspace = workspace
+            self._keep += list(workspace)
+            self._step_args = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                               _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                               _ptr(context_lens), ctypes.c_float(scale),
+                               ctypes.c_int32(self.partition_size),
+                               ctypes.c_int32(self.num_partitions), _ptr(tmp), _ptr(ml),
+                               _ptr(es), _ptr(counters), _ptr(self.out), sref)
         else:
             if workspace is None:
                 workspace = split_workspace(q, self.num_partitions)
@@ -380,11 +492,15 @@ class StepPlan:
         return ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
 
     def reshape_and_cache(self):
+        if self.mode == "fused":
+            return                          # part of the fused step
         _check("pa_reshape_and_cache",
                self._lib.pa_reshape_and_cache(*self._reshape_args, self._stream()))
 
     def decode(self):
-        if self.mode == "single":
+        if self.mode == "fused":
+            _check("pa_decode_step", self._lib.pa_decode_step(*self._step_args, self._stream()))
+        elif self.mode == "single":
             _check("pa_decode", self._lib.pa_decode(*self._decode_args, self._stream()))
         else:
             _check("pa_decode_split",

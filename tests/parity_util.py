@@ -42,7 +42,7 @@ def gpu_bits(t: torch.Tensor) -> np.ndarray:
     return pin.bits(t.cpu())
 
 
-def check_workload(w: pin.Workload, dev, modes=("single", "split"), partition_size=512,
+def check_workload(w: pin.Workload, dev, modes=("single", "split", "fused"), partition_size=512,
                    check_partitions=True):
     """Cache write bit-exact, then decode through each mode against the oracle.
     Returns a dict of max errors."""
@@ -60,6 +60,21 @@ def check_workload(w: pin.Workload, dev, modes=("single", "split"), partition_si
     errs = {}
     max_len = int(w.context_lens.max()) if w.num_seqs else 0
     for mode in modes:
+        if mode == "fused":
+            # one launch from the unwritten caches: cache write + attention + merge
+            kc = w.k_cache.to(dev)
+            vc = w.v_cache.to(dev)
+            S = lib.num_partitions(max_len, partition_size)
+            ws = lib.step_workspace(d["q"], w.num_kv_heads, S)
+            out = lib.decode_step(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], kc, vc,
+                                  d["block_tables"], d["context_lens"], w.scale, max_len,
+                                  partition_size=partition_size, workspace=ws)
+            torch.cuda.synchronize(dev)
+            assert np.array_equal(gpu_bits(kc), kc_ref), "fused step: k_cache differs"
+            assert np.array_equal(gpu_bits(vc), vc_ref), "fused step: v_cache differs"
+            assert int(ws[3].abs().sum()) == 0, "fused step left counters non-zero"
+            errs[mode] = assert_close(out.float().cpu().numpy(), want, f"{w.name} fused out")
+            continue
         if mode == "single":
             out = lib.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                              d["context_lens"], w.scale)

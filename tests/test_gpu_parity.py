@@ -52,7 +52,7 @@ def test_edge_lengths(dev, dtype, hq, hkv, d, bs):
                                        num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                                        block_size=bs), seed=hq * 7 + d + bs)
     for P in sorted({bs, 2 * bs, 64 if 64 % bs == 0 else bs, 512}):
-        check_workload(w, dev, modes=("split",), partition_size=P)
+        check_workload(w, dev, modes=("split", "fused"), partition_size=P)
     check_workload(w, dev, modes=("single",))
 
 
@@ -145,7 +145,7 @@ def test_non_default_stream(dev):
     assert_close(out.float().cpu().numpy(), want, "side stream")
 
 
-@pytest.mark.parametrize("mode", ["single", "split"])
+@pytest.mark.parametrize("mode", ["single", "split", "fused"])
 def test_step_plan_eager_and_graph_replay(dev, mode):
     """The prepared step (and its CUDA-graph replay) equals the plain calls."""
     w = pin.build_workload(params=dict(dtype="bf16", num_seqs=9, lens=[1, 16, 33, 100, 600, 1000,
@@ -168,4 +168,69 @@ def test_step_plan_eager_and_graph_replay(dev, mode):
         got = plan.replay()
     torch.cuda.synchronize(dev)
     assert torch.equal(got, eager)
+    assert lib.read_device_errors(dev) == 0
+
+
+def test_fused_step_rejects_a_slot_that_is_not_the_last_position(dev):
+    """A slot other than position L-1's is not written; attention runs on the
+    cache as it was, and the device error word reports it."""
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=3, lens=[5, 40, 700],
+                                       num_q_heads=8, num_kv_heads=2, head_dim=128,
+                                       block_size=16), seed=31)
+    slots = w.slot_mapping.copy()
+    slots[1] = slots[1] - 1                      # points at position L-2
+    d = to_device(w, dev)
+    d["slot_mapping"] = torch.from_numpy(slots).to(dev)
+    before_k = d["k_cache"].clone()
+    lib.read_device_errors(dev)
+    out = lib.decode_step(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
+                          d["v_cache"], d["block_tables"], d["context_lens"], w.scale, 700)
+    torch.cuda.synchronize(dev)
+    assert lib.read_device_errors(dev) & lib.PA_DEVERR_BAD_SLOT
+    # sequences 0 and 2 got their token written; sequence 1 did not
+    keep = slots.copy()
+    keep[1] = -1
+    kc, vc, _ = oracle.reshape_and_cache(pin.bits(w.k_new), pin.bits(w.v_new), keep,
+                                         pin.bits(w.k_cache), pin.bits(w.v_cache), w.block_size)
+    assert np.array_equal(pin.bits(d["k_cache"].cpu()), kc)
+    assert not torch.equal(before_k, d["k_cache"])
+    want = oracle.paged_decode(pin.bits(w.q), kc, vc, w.block_tables, w.context_lens, w.scale,
+                               w.dtype)
+    assert_close(out.float().cpu().numpy(), want, "fused step with a rejected slot")
+
+
+def test_fused_step_back_to_back_steps(dev):
+    """Consecutive steps reuse the counters; each step appends one token."""
+    w = pin.build_workload(params=dict(dtype="bf16", num_seqs=4, lens=[1, 29, 600, 1300],
+                                       num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                       block_size=16), seed=41)
+    d = to_device(w, dev)
+    ws = lib.step_workspace(d["q"], w.num_kv_heads, lib.num_partitions(2048, 512))
+    kc, vc = pin.bits(w.k_cache), pin.bits(w.v_cache)
+    lens = w.context_lens.copy()
+    for step in range(3):
+        if step:
+            # next token: the allocator's slot for position L (same block unless it filled)
+            lens = lens + 1
+            slots = np.array([w.block_tables[b, (L - 1) // 16] * 16 + (L - 1) % 16
+                              for b, L in enumerate(lens)], dtype=np.int64)
+            if np.any((lens - 1) // 16 >= w.block_tables.shape[1]):
+                break
+            d["context_lens"] = torch.from_numpy(lens.astype(np.int32)).to(dev)
+            d["slot_mapping"] = torch.from_numpy(slots).to(dev)
+            rng = np.random.default_rng(step)
+            kn = pin.normal_tensor(rng, tuple(w.k_new.shape), "bf16")
+            vn = pin.normal_tensor(rng, tuple(w.v_new.shape), "bf16")
+        else:
+            slots, kn, vn = w.slot_mapping, w.k_new, w.v_new
+        d["k_new"], d["v_new"] = kn.to(dev), vn.to(dev)
+        out = lib.decode_step(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
+                              d["v_cache"], d["block_tables"], d["context_lens"], w.scale, 2048,
+                              workspace=ws)
+        kc, vc, _ = oracle.reshape_and_cache(pin.bits(kn), pin.bits(vn), slots, kc, vc,
+                                             w.block_size)
+        want = oracle.paged_decode(pin.bits(w.q), kc, vc, w.block_tables, lens, w.scale,
+                                   w.dtype)
+        assert_close(out.float().cpu().numpy(), want, f"fused step {step}")
+        assert int(ws[3].abs().sum()) == 0
     assert lib.read_device_errors(dev) == 0
