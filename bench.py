@@ -39,6 +39,7 @@ from paged_kv_cache_226_gb300 import lib  # noqa: E402
 METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; µs per layer-step"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+FP8_K_SCALE, FP8_V_SCALE = 1.0 / 64, 1.0 / 48
 DECODE_KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_226_gb300", "csrc", "decode_kernel.cuh")
 
 
@@ -94,15 +95,15 @@ def profiled_traffic(config: str, kernel: str):
     return p.get("dram_bytes_per_launch")
 
 
-def step_bytes(w: pin.Workload, mode: str, partition: int):
+def step_bytes(w: pin.Workload, mode: str, partition: int, cache_elem_bytes: int = 2):
     """Algorithmic bytes: the layer-step and each kernel of it."""
     e = 2
     B, hq, hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
-    kv = w.kv_bytes_logical()
+    kv = w.kv_bytes_logical() * cache_elem_bytes // 2
     q = B * hq * d * e
     out = B * hq * d * e
     new_tok = w.num_tokens * hkv * d * e * 2           # read k, v
-    write_tok = int((w.slot_mapping >= 0).sum()) * hkv * d * e * 2
+    write_tok = int((w.slot_mapping >= 0).sum()) * hkv * d * cache_elem_bytes * 2
     parts = sum(-(-int(L) // partition) for L in w.context_lens)
     split_w = parts * hq * (d + 2) * 4                  # tmp_out + max_logits + exp_sums
     kernels = {"reshape_and_cache": new_tok + write_tok + w.num_tokens * 8}
@@ -113,7 +114,7 @@ def step_bytes(w: pin.Workload, mode: str, partition: int):
         kernels["lse_reduce"] = split_w + out
     else:
         kernels["paged_decode"] = kv + q + out
-    return {"layer_step": kv + q + out, "kernels": kernels, "partitions": parts}
+    return {"layer_step": kv + q + out, "kernels": kernels, "partitions": parts, "kv": kv}
 
 
 class ClockSampler:
@@ -317,17 +318,25 @@ def bench_ours(args):
                                                        w.block_size, dev)
     S = lib.num_partitions(max_len, partition)
 
+    kc, vc, scales = w.k_cache, w.v_cache, {}
+    if args.kv_dtype == "fp8":
+        if mode != "fused":
+            raise SystemExit("--kv-dtype fp8 runs the fused step")
+        rng = np.random.default_rng(rank_seed(args.config, rank) + 7)
+        kc = pin.fp8_codes(rng, tuple(w.k_cache.shape), FP8_K_SCALE)
+        vc = pin.fp8_codes(rng, tuple(w.v_cache.shape), FP8_V_SCALE)
+        scales = dict(k_scale=FP8_K_SCALE, v_scale=FP8_V_SCALE)
     d = {k: v.to(dev) for k, v in dict(
-        q=w.q, k_new=w.k_new, v_new=w.v_new, k_cache=w.k_cache, v_cache=w.v_cache,
+        q=w.q, k_new=w.k_new, v_new=w.v_new, k_cache=kc, v_cache=vc,
         block_tables=torch.from_numpy(w.block_tables),
         context_lens=torch.from_numpy(w.context_lens),
         slot_mapping=torch.from_numpy(w.slot_mapping)).items()}
     plan = lib.StepPlan(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
                         d["v_cache"], d["block_tables"], d["context_lens"], w.scale, max_len,
-                        mode=mode, partition_size=partition)
+                        mode=mode, partition_size=partition, **scales)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
-    nb = step_bytes(w, mode, partition)
+    nb = step_bytes(w, mode, partition, 1 if args.kv_dtype == "fp8" else 2)
 
     for _ in range(args.warmup):
         flush(1.0)
@@ -430,14 +439,16 @@ def bench_ours(args):
         "us_per_layer_step": round(ms * 1e3, 2),
         "hbm_frac_of_measured" if peak_src == "measured" else "hbm_frac_of_fallback":
             round(value / world / hbm, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype if args.kv_dtype != "fp8" else f"{w.dtype} (q, out), e4m3 (K/V cache)",
         "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
         "config": {"workload": f"{w.name}: {pin.DESCRIPTIONS[w.name]}"
                                + (f" with {args.params}" if args.params else ""), "mode": mode,
                    "partition_tokens": partition if mode != "single" else None,
                    "l2": "flushed before every step (256 MiB write, then 256 MiB read of another "
                          "buffer; outside the step's events)",
-                   "kv_bytes": w.kv_bytes_logical(), "kv_bytes_unique": w.kv_bytes_unique(),
+                   "kv_bytes": nb["kv"], "kv_bytes_unique": w.kv_bytes_unique() * (
+                       1 if args.kv_dtype != "fp8" else 0.5),
                    "bytes_per_step": nb["layer_step"], "seqs_per_gpu": w.num_seqs},
         "kernels_us": {**({} if mode == "fused" else
                           {"reshape_and_cache": round(1e3 * sum(k1_ms) / len(k1_ms), 2)}),
@@ -476,6 +487,8 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=0,
                     help="tokens per partition (0: chosen from the batch shape)")
     ap.add_argument("--params", default="", help="JSON overrides of the workload parameters")
+    ap.add_argument("--kv-dtype", default="auto", choices=["auto", "fp8"],
+                    help="cache element type: the workload's fp16/bf16, or E4M3 codes")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -157,6 +157,46 @@ int pa_reduce(const float* tmp_out, const float* max_logits, const float* exp_su
               int32_t max_num_partitions, void* out, const pa_shape* shp, void* stream);
 
 /*
+ * FP8 KV cache.  The pages name the KV-cache data type as a knob that, like
+ * weight quantisation, shrinks the KV pool so that more requests fit
+ * (ta-paperlens page, --quantization / --kv-cache-dtype; youngju.dev post,
+ * quantisation section).  Here the cache holds OCP E4M3 codes (1 byte per
+ * element, [num_blocks][block_size][num_kv_heads][head_dim] bytes) with one
+ * scale per tensor: element = e4m3(code) * k_scale (K) or * v_scale (V).
+ * q, k, v (new tokens) and out keep the 16-bit type of shp->dtype.
+ * head_dim must be 128 (else PA_ERR_UNSUPPORTED); scales must be finite and
+ * > 0 (else PA_ERR_INVALID_ARG).  Otherwise these mirror the 16-bit entry
+ * points, argument for argument, with the scales added.
+ *
+ * pa_reshape_and_cache_fp8: code = E4M3 of x / k_scale (x / v_scale), the
+ * quotient in fp32, rounded to nearest even, saturating at +-448.
+ */
+int pa_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                             void* k_cache, void* v_cache, int64_t num_tokens, float k_scale,
+                             float v_scale, const pa_shape* shp, void* stream);
+
+/* pa_decode over an E4M3 cache. */
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, float scale,
+                  float k_scale, float v_scale, void* out, const pa_shape* shp, void* stream);
+
+/* pa_decode_split over an E4M3 cache (merge the partitions with pa_reduce). */
+int pa_decode_split_fp8(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale,
+                        float k_scale, float v_scale, int32_t partition_size,
+                        int32_t max_num_partitions, float* tmp_out, float* max_logits,
+                        float* exp_sums, const pa_shape* shp, void* stream);
+
+/* pa_decode_step over an E4M3 cache: the new token is quantised as in
+ * pa_reshape_and_cache_fp8 and attention reads the quantised values. */
+int pa_decode_step_fp8(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                       void* k_cache, void* v_cache, const int32_t* block_tables,
+                       const int32_t* context_lens, float scale, float k_scale, float v_scale,
+                       int32_t partition_size, int32_t max_num_partitions, float* tmp_out,
+                       float* max_logits, float* exp_sums, int32_t* counters, void* out,
+                       const pa_shape* shp, void* stream);
+
+/*
  * pa_copy_blocks: copy whole physical blocks between two block pools.  For
  * each pair p < num_pairs of block_mapping (int64 [num_pairs][2], device):
  *   src = block_mapping[2p], dst = block_mapping[2p+1],

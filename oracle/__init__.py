@@ -69,6 +69,16 @@ def _load():
             lib.oracle_contiguous_decode.restype = i32
             lib.oracle_contiguous_decode.argtypes = [P, P, P, P, P, f64, i32, i32, i32, i32,
                                                      i32, P]
+            lib.oracle_e4m3_to_f64.restype = f64
+            lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+            lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+            lib.oracle_reshape_and_cache_fp8.restype = i64
+            lib.oracle_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i64,
+                                                         i32, ctypes.c_float, ctypes.c_float]
+            lib.oracle_paged_decode_fp8.restype = i32
+            lib.oracle_paged_decode_fp8.argtypes = [P, P, P, P, P, f64, f64, f64, i32, i32, i32,
+                                                    i32, i32, i32, i32, P]
             lib.oracle_copy_blocks.restype = i64
             lib.oracle_copy_blocks.argtypes = [P, P, i64, P, P, i64, P, i64, i32, i32, i32]
             lib.oracle_max_threads.restype = i32
@@ -173,6 +183,52 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, block_size: int):
     bad = _load().oracle_reshape_and_cache(_ptr(k), _ptr(v), _ptr(sm), _ptr(kc), _ptr(vc),
                                            T, hkv, d, bs, nb)
     return kc, vc, int(bad)
+
+
+def e4m3_to_f64(code: int) -> float:
+    return float(_load().oracle_e4m3_to_f64(int(code)))
+
+
+def f32_to_e4m3(y: float) -> int:
+    """Nearest E4M3 code (ties to even, saturating at 448) of float32(y)."""
+    return int(_load().oracle_f32_to_e4m3(float(np.float32(y))))
+
+
+def reshape_and_cache_fp8(k, v, slot_mapping, k_cache, v_cache, block_size: int, dtype: str,
+                          k_scale: float, v_scale: float):
+    """FP8 cache write: returns (k_cache', v_cache', n_out_of_pool); caches
+    are uint8 [NB][bs][Hkv][D] (copied, not modified)."""
+    k, v = _u16(k), _u16(v)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8).copy()
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8).copy()
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T = sm.shape[0]
+    nb, bs, hkv, d = kc.shape
+    assert bs == block_size and k.shape == (T, hkv, d) and v.shape == (T, hkv, d)
+    bad = _load().oracle_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(sm), _ptr(kc), _ptr(vc),
+                                               T, hkv, d, bs, nb, _DTYPES[dtype],
+                                               float(k_scale), float(v_scale))
+    return kc, vc, int(bad)
+
+
+def paged_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                     k_scale: float, v_scale: float, dtype: str) -> np.ndarray:
+    """fp64 attention over an E4M3 cache (uint8 [NB][bs][Hkv][D])."""
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = kc.shape
+    assert d2 == d and vc.shape == kc.shape and cl.shape == (B,) and bt.shape[0] == B
+    out = np.zeros((B, hq, d), dtype=np.float64)
+    rc = _load().oracle_paged_decode_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl),
+                                         float(scale), float(k_scale), float(v_scale), B, hq,
+                                         hkv, d, bs, bt.shape[1], _DTYPES[dtype], _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_paged_decode_fp8: bad shape")
+    return out
 
 
 def copy_blocks(k_src, v_src, k_dst, v_dst, mapping):

@@ -75,6 +75,45 @@ double oracle_bf16_to_f64(uint16_t h) {
     return sign ? -v : v;
 }
 
+/* OCP FP8 E4M3 (the "fn" variant): 1 sign, 4 exponent (bias 7), 3 fraction
+ * bits; no infinities; S.1111.111 is NaN; largest finite 448. */
+double oracle_e4m3_to_f64(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 0x7;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -9);                /* subnormal: f/8 * 2^-6 */
+    } else if (e == 15 && f == 7) {
+        v = NAN;
+    } else {
+        v = ldexp(8.0 + (double)f, e - 10);      /* (1 + f/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+/*
+ * Nearest E4M3 code of a float, ties to the even code, magnitudes above 448
+ * saturated to 448, NaN to the NaN code.  Found by comparing against every
+ * finite positive code (exact in double).
+ */
+uint8_t oracle_f32_to_e4m3(float y) {
+    if (y != y) return 0x7f;
+    uint8_t sign = (y < 0.0f || (y == 0.0f && 1.0f / y < 0.0f)) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+    int best = 0;
+    double best_err = a;                         /* code 0 is +0 */
+    for (int c = 1; c <= 0x7e; ++c) {
+        double err = fabs(oracle_e4m3_to_f64((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
 static double widen(uint16_t h, int dtype) {
     return dtype == OR_DTYPE_BF16 ? oracle_bf16_to_f64(h) : oracle_f16_to_f64(h);
 }
@@ -109,6 +148,33 @@ int64_t oracle_reshape_and_cache(const uint16_t* k, const uint16_t* v,
         int64_t dst = (blk * block_size + off) * row;
         memcpy(k_cache + dst, k + t * row, (size_t)row * sizeof(uint16_t));
         memcpy(v_cache + dst, v + t * row, (size_t)row * sizeof(uint16_t));
+    }
+    return bad;
+}
+
+/*
+ * FP8 cache write: each element of the new token's K (V) becomes the E4M3
+ * code of x / k_scale (x / v_scale), the quotient taken in fp32.  Slots as
+ * in oracle_reshape_and_cache.  Caches are [num_blocks][block_size][Hkv][D]
+ * bytes.  Returns the number of tokens whose slot lies past the pool.
+ */
+int64_t oracle_reshape_and_cache_fp8(const uint16_t* k, const uint16_t* v,
+                                     const int64_t* slot_mapping, uint8_t* k_cache,
+                                     uint8_t* v_cache, int64_t num_tokens, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks,
+                                     int dtype, float k_scale, float v_scale) {
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    int64_t bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        if (s / block_size >= num_blocks) { ++bad; continue; }
+        for (int64_t i = 0; i < row; ++i) {
+            float xk = (float)widen(k[t * row + i], dtype);
+            float xv = (float)widen(v[t * row + i], dtype);
+            k_cache[s * row + i] = oracle_f32_to_e4m3(xk / k_scale);
+            v_cache[s * row + i] = oracle_f32_to_e4m3(xv / v_scale);
+        }
     }
     return bad;
 }
@@ -271,6 +337,56 @@ int oracle_paged_decode_partitions(const uint16_t* q, const uint16_t* k_cache,
                         part_out + idx * head_dim, part_max + idx, part_sum + idx);
         }
         free(qrow);
+    }
+    return 0;
+}
+
+/*
+ * Paged decode attention over an FP8 (E4M3) cache with per-tensor scales:
+ * K_i = e4m3(code) * k_scale, V_i = e4m3(code) * v_scale, then the same
+ * two-pass softmax definition as oracle_paged_decode.  q is 16-bit (dtype).
+ */
+int oracle_paged_decode_fp8(const uint16_t* q, const uint8_t* k_cache,
+                            const uint8_t* v_cache, const int32_t* block_tables,
+                            const int32_t* context_lens, double scale, double k_scale,
+                            double v_scale, int num_seqs, int num_q_heads, int num_kv_heads,
+                            int head_dim, int block_size, int max_blocks_per_seq, int dtype,
+                            double* out) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
+    int G = num_q_heads / num_kv_heads;
+    int64_t pairs = (int64_t)num_seqs * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < pairs; ++bh) {
+        int b = (int)(bh / num_q_heads);
+        int g = (int)(bh % num_q_heads) / G;
+        const int32_t* table = block_tables + (int64_t)b * max_blocks_per_seq;
+        int64_t L = context_lens[b];
+        double* o = out + bh * head_dim;
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        if (L <= 0) continue;
+        double* s = (double*)malloc((size_t)L * sizeof(double));
+        double m = -INFINITY;
+        for (int64_t i = 0; i < L; ++i) {
+            int64_t base = ((int64_t)table[i / block_size] * block_size + i % block_size) *
+                               num_kv_heads * head_dim + (int64_t)g * head_dim;
+            double dot = 0.0;
+            for (int d = 0; d < head_dim; ++d)
+                dot += widen(q[bh * head_dim + d], dtype) *
+                       (oracle_e4m3_to_f64(k_cache[base + d]) * k_scale);
+            s[i] = scale * dot;
+            if (s[i] > m) m = s[i];
+        }
+        double l = 0.0;
+        for (int64_t i = 0; i < L; ++i) {
+            int64_t base = ((int64_t)table[i / block_size] * block_size + i % block_size) *
+                               num_kv_heads * head_dim + (int64_t)g * head_dim;
+            double w = exp(s[i] - m);
+            l += w;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] += w * (oracle_e4m3_to_f64(v_cache[base + d]) * v_scale);
+        }
+        for (int d = 0; d < head_dim; ++d) o[d] /= l;
+        free(s);
     }
     return 0;
 }

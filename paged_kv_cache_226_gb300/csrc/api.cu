@@ -88,27 +88,38 @@ int check_shape(const pa_shape* s, bool need_q_heads) {
     return PA_OK;
 }
 
-// 4-D view [num_blocks][block_size][Hkv][D] of a cache; box = 64 dims x one
-// head x 16 tokens x one block, 128 B swizzle (conflict-free ldmatrix rows).
-int encode_cache_map(CUtensorMap* map, const void* base, const pa_shape* s) {
+// 4-D view [num_blocks][block_size][Hkv][D] of a cache; box = one 128-byte
+// row slice (64 dims of a 16-bit cache, 128 dims of an FP8 one) x one head x
+// 16 tokens x one block, 128 B swizzle (conflict-free ldmatrix rows).
+int encode_cache_map(CUtensorMap* map, const void* base, const pa_shape* s, bool fp8) {
     EncodeTiledFn enc = nullptr;
     cudaError_t e = get_encoder(&enc);
     if (e != cudaSuccess) return cuda_fail(e);
-    const cuuint64_t elem = 2;
+    const cuuint64_t elem = fp8 ? 1 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)s->head_dim, (cuuint64_t)s->num_kv_heads,
                           (cuuint64_t)s->block_size, (cuuint64_t)s->num_blocks};
     cuuint64_t strides[3] = {s->head_dim * elem, (cuuint64_t)s->num_kv_heads * s->head_dim * elem,
                              (cuuint64_t)s->block_size * s->num_kv_heads * s->head_dim * elem};
-    cuuint32_t box[4] = {(cuuint32_t)pa::kBoxElems, 1, (cuuint32_t)pa::kTileTokens, 1};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / elem), 1, (cuuint32_t)pa::kTileTokens, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUtensorMapDataType dt = s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : (s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
     CUresult r = enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return PA_ERR_INVALID_ARG;
     return PA_OK;
 }
+
+// How the cache stores K and V: the 16-bit type of shp->dtype, or E4M3 bytes
+// with per-tensor scales.
+struct CacheKind {
+    bool fp8;
+    float k_scale;
+    float v_scale;
+};
+constexpr CacheKind kCache16 = {false, 1.f, 1.f};
 
 int check_decode_args(const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* context_lens,
@@ -125,13 +136,15 @@ int check_decode_args(const void* q, const void* k_cache, const void* v_cache,
 
 pa::DecodeParams make_params(const void* q, const int32_t* block_tables,
                              const int32_t* context_lens, float scale, const pa_shape* shp,
-                             int* err) {
+                             int* err, const CacheKind& ck) {
     pa::DecodeParams p{};
     p.q = q;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.err = err;
-    p.scale_log2 = scale * pa::kLog2e;
+    p.scale_log2 = scale * ck.k_scale * pa::kLog2e;
+    p.k_scale = ck.k_scale;
+    p.v_scale = ck.v_scale;
     p.num_q_heads = shp->num_q_heads;
     p.group = shp->num_q_heads / shp->num_kv_heads;
     p.max_blocks_per_seq = shp->max_blocks_per_seq;
@@ -199,25 +212,134 @@ int pa_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mappi
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
-int pa_decode(const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_tables, const int32_t* context_lens, float scale,
-              void* out, const pa_shape* shp, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int check_kind(const pa_shape* shp, const CacheKind& ck) {
+    if (!ck.fp8) return PA_OK;
+    if (shp->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (!(ck.k_scale > 0.f) || !(ck.v_scale > 0.f) || ck.k_scale == INFINITY ||
+        ck.v_scale == INFINITY)
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+cudaError_t launch(int mode, const pa_shape* shp, const CacheKind& ck, const CUtensorMap& tmk,
+                   const CUtensorMap& tmv, const pa::DecodeParams& p, dim3 grid, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ck.fp8) return pa::launch_decode_fp8(shp->dtype, mode, tmk, tmv, p, grid, s);
+    return pa::launch_decode(shp->dtype, shp->head_dim, mode, tmk, tmv, p, grid, s);
+}
+
+int decode_single(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, float scale,
+                  void* out, const pa_shape* shp, void* stream, const CacheKind& ck) {
     int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
     if (st != PA_OK) return st;
+    if ((st = check_kind(shp, ck)) != PA_OK) return st;
     if (shp->num_seqs == 0) return PA_OK;
     if (!out || !aligned16(out)) return PA_ERR_INVALID_ARG;
     CUtensorMap tmk, tmv;
-    if ((st = encode_cache_map(&tmk, k_cache, shp)) != PA_OK) return st;
-    if ((st = encode_cache_map(&tmv, v_cache, shp)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmk, k_cache, shp, ck.fp8)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp, ck.fp8)) != PA_OK) return st;
     int* err = nullptr;
     cudaError_t e = error_word(&err);
     if (e != cudaSuccess) return cuda_fail(e);
-    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err);
+    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err, ck);
     p.out = out;
-    dim3 grid(1, shp->num_kv_heads, shp->num_seqs);
-    e = pa::launch_decode(shp->dtype, shp->head_dim, pa::kModeSingle, tmk, tmv, p, grid,
-                          static_cast<cudaStream_t>(stream));
+    dim3 grid(shp->num_seqs, shp->num_kv_heads, 1);
+    e = launch(pa::kModeSingle, shp, ck, tmk, tmv, p, grid, stream);
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int decode_split(const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, float scale,
+                 int32_t partition_size, int32_t max_num_partitions, float* tmp_out,
+                 float* max_logits, float* exp_sums, const pa_shape* shp, void* stream,
+                 const CacheKind& ck) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if ((st = check_kind(shp, ck)) != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
+    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
+    if (max_num_partitions > 65535) return PA_ERR_UNSUPPORTED;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!tmp_out || !max_logits || !exp_sums) return PA_ERR_WORKSPACE;
+    if (!aligned16(tmp_out) || !aligned16(max_logits) || !aligned16(exp_sums))
+        return PA_ERR_INVALID_ARG;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp, ck.fp8)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp, ck.fp8)) != PA_OK) return st;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err, ck);
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.partition_tokens = partition_size;
+    p.max_parts = max_num_partitions;
+    dim3 grid(shp->num_seqs, shp->num_kv_heads, max_num_partitions);
+    e = launch(pa::kModeSplit, shp, ck, tmk, tmv, p, grid, stream);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int decode_step(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                void* k_cache, void* v_cache, const int32_t* block_tables,
+                const int32_t* context_lens, float scale, int32_t partition_size,
+                int32_t max_num_partitions, float* tmp_out, float* max_logits, float* exp_sums,
+                int32_t* counters, void* out, const pa_shape* shp, void* stream,
+                const CacheKind& ck) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if ((st = check_kind(shp, ck)) != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
+    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !out || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    if (!tmp_out || !max_logits || !exp_sums || !counters) return PA_ERR_WORKSPACE;
+    if (!aligned16(tmp_out) || !aligned16(max_logits) || !aligned16(exp_sums) ||
+        (reinterpret_cast<uintptr_t>(counters) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int G = shp->num_q_heads / shp->num_kv_heads;
+    if ((int64_t)G * max_num_partitions + G > pa::decode_merge_floats(shp->head_dim))
+        return PA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp, ck.fp8)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp, ck.fp8)) != PA_OK) return st;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err, ck);
+    p.out = out;
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.partition_tokens = partition_size;
+    p.max_parts = max_num_partitions;
+    p.k_new = k;
+    p.v_new = v;
+    p.slot_mapping = slot_mapping;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.counters = counters;
+    dim3 grid(shp->num_seqs, shp->num_kv_heads, max_num_partitions);
+    e = launch(pa::kModeStep, shp, ck, tmk, tmv, p, grid, stream);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode(const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale,
+              void* out, const pa_shape* shp, void* stream) {
+    return decode_single(q, k_cache, v_cache, block_tables, context_lens, scale, out, shp,
+                         stream, kCache16);
 }
 
 size_t pa_split_workspace_size(const pa_shape* shp, int32_t max_context_len,
@@ -234,30 +356,9 @@ int pa_decode_split(const void* q, const void* k_cache, const void* v_cache,
                     const int32_t* block_tables, const int32_t* context_lens, float scale,
                     int32_t partition_size, int32_t max_num_partitions, float* tmp_out,
                     float* max_logits, float* exp_sums, const pa_shape* shp, void* stream) {
-    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
-    if (st != PA_OK) return st;
-    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
-    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
-    if (shp->num_seqs == 0) return PA_OK;
-    if (!tmp_out || !max_logits || !exp_sums) return PA_ERR_WORKSPACE;
-    if (!aligned16(tmp_out) || !aligned16(max_logits) || !aligned16(exp_sums))
-        return PA_ERR_INVALID_ARG;
-    CUtensorMap tmk, tmv;
-    if ((st = encode_cache_map(&tmk, k_cache, shp)) != PA_OK) return st;
-    if ((st = encode_cache_map(&tmv, v_cache, shp)) != PA_OK) return st;
-    int* err = nullptr;
-    cudaError_t e = error_word(&err);
-    if (e != cudaSuccess) return cuda_fail(e);
-    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err);
-    p.tmp_out = tmp_out;
-    p.max_logits = max_logits;
-    p.exp_sums = exp_sums;
-    p.partition_tokens = partition_size;
-    p.max_parts = max_num_partitions;
-    dim3 grid(max_num_partitions, shp->num_kv_heads, shp->num_seqs);
-    e = pa::launch_decode(shp->dtype, shp->head_dim, pa::kModeSplit, tmk, tmv, p, grid,
-                          static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+    return decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, partition_size,
+                        max_num_partitions, tmp_out, max_logits, exp_sums, shp, stream,
+                        kCache16);
 }
 
 int pa_decode_step(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
@@ -266,44 +367,59 @@ int pa_decode_step(const void* q, const void* k, const void* v, const int64_t* s
                    int32_t max_num_partitions, float* tmp_out, float* max_logits,
                    float* exp_sums, int32_t* counters, void* out, const pa_shape* shp,
                    void* stream) {
-    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    return decode_step(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, scale,
+                       partition_size, max_num_partitions, tmp_out, max_logits, exp_sums,
+                       counters, out, shp, stream, kCache16);
+}
+
+int pa_reshape_and_cache_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                             void* k_cache, void* v_cache, int64_t num_tokens, float k_scale,
+                             float v_scale, const pa_shape* shp, void* stream) {
+    int st = check_shape(shp, false);
     if (st != PA_OK) return st;
-    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
-    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
-    if (shp->num_seqs == 0) return PA_OK;
-    if (!k || !v || !slot_mapping || !out || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+    if ((st = check_kind(shp, CacheKind{true, k_scale, v_scale})) != PA_OK) return st;
+    if (num_tokens < 0 || num_tokens > 0x7fffffffll) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
         (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return PA_ERR_INVALID_ARG;
-    if (!tmp_out || !max_logits || !exp_sums || !counters) return PA_ERR_WORKSPACE;
-    if (!aligned16(tmp_out) || !aligned16(max_logits) || !aligned16(exp_sums) ||
-        (reinterpret_cast<uintptr_t>(counters) & 3u))
-        return PA_ERR_INVALID_ARG;
-    const int G = shp->num_q_heads / shp->num_kv_heads;
-    if ((int64_t)G * max_num_partitions + G > pa::decode_merge_floats(shp->head_dim))
-        return PA_ERR_UNSUPPORTED;
-    CUtensorMap tmk, tmv;
-    if ((st = encode_cache_map(&tmk, k_cache, shp)) != PA_OK) return st;
-    if ((st = encode_cache_map(&tmv, v_cache, shp)) != PA_OK) return st;
     int* err = nullptr;
     cudaError_t e = error_word(&err);
     if (e != cudaSuccess) return cuda_fail(e);
-    pa::DecodeParams p = make_params(q, block_tables, context_lens, scale, shp, err);
-    p.out = out;
-    p.tmp_out = tmp_out;
-    p.max_logits = max_logits;
-    p.exp_sums = exp_sums;
-    p.partition_tokens = partition_size;
-    p.max_parts = max_num_partitions;
-    p.k_new = k;
-    p.v_new = v;
-    p.slot_mapping = slot_mapping;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
-    p.counters = counters;
-    dim3 grid(max_num_partitions, shp->num_kv_heads, shp->num_seqs);
-    e = pa::launch_decode(shp->dtype, shp->head_dim, pa::kModeStep, tmk, tmv, p, grid,
-                          static_cast<cudaStream_t>(stream));
+    e = pa::launch_reshape_and_cache_fp8(shp->dtype, k, v, slot_mapping, k_cache, v_cache,
+                                         num_tokens, shp->num_blocks * shp->block_size,
+                                         shp->num_kv_heads * shp->head_dim, k_scale, v_scale,
+                                         err, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+int pa_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, float scale,
+                  float k_scale, float v_scale, void* out, const pa_shape* shp, void* stream) {
+    return decode_single(q, k_cache, v_cache, block_tables, context_lens, scale, out, shp,
+                         stream, CacheKind{true, k_scale, v_scale});
+}
+
+int pa_decode_split_fp8(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens, float scale,
+                        float k_scale, float v_scale, int32_t partition_size,
+                        int32_t max_num_partitions, float* tmp_out, float* max_logits,
+                        float* exp_sums, const pa_shape* shp, void* stream) {
+    return decode_split(q, k_cache, v_cache, block_tables, context_lens, scale, partition_size,
+                        max_num_partitions, tmp_out, max_logits, exp_sums, shp, stream,
+                        CacheKind{true, k_scale, v_scale});
+}
+
+int pa_decode_step_fp8(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                       void* k_cache, void* v_cache, const int32_t* block_tables,
+                       const int32_t* context_lens, float scale, float k_scale, float v_scale,
+                       int32_t partition_size, int32_t max_num_partitions, float* tmp_out,
+                       float* max_logits, float* exp_sums, int32_t* counters, void* out,
+                       const pa_shape* shp, void* stream) {
+    return decode_step(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, scale,
+                       partition_size, max_num_partitions, tmp_out, max_logits, exp_sums,
+                       counters, out, shp, stream, CacheKind{true, k_scale, v_scale});
 }
 
 int pa_copy_blocks(const void* k_src, const void* v_src, int64_t src_num_blocks, void* k_dst,

@@ -9,6 +9,18 @@ cudaError_t launch_decode_f16(int, int, const CUtensorMap&, const CUtensorMap&,
 cudaError_t launch_decode_bf16(int, int, const CUtensorMap&, const CUtensorMap&,
                                const DecodeParams&, dim3, cudaStream_t);
 
+cudaError_t launch_decode_fp8_f16(int, const CUtensorMap&, const CUtensorMap&,
+                                  const DecodeParams&, dim3, cudaStream_t);
+cudaError_t launch_decode_fp8_bf16(int, const CUtensorMap&, const CUtensorMap&,
+                                   const DecodeParams&, dim3, cudaStream_t);
+
+cudaError_t launch_decode_fp8(int dtype, int mode, const CUtensorMap& tmk,
+                              const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
+                              cudaStream_t stream) {
+    if (dtype == PA_BF16) return launch_decode_fp8_bf16(mode, tmk, tmv, p, grid, stream);
+    return launch_decode_fp8_f16(mode, tmk, tmv, p, grid, stream);
+}
+
 cudaError_t launch_decode(int dtype, int head_dim, int mode, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
                           cudaStream_t stream) {
@@ -59,6 +71,59 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int64_t
                            stream, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
                            slots, static_cast<uint4*>(kc), static_cast<uint4*>(vc), num_slots,
                            vec, err);
+}
+
+// FP8 cache write: every element becomes the E4M3 code of x / scale (the
+// quotient in fp32, round to nearest even, saturating at +-448).  One CTA per
+// token; each thread converts 8 elements (16 bytes in, 8 bytes out).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                 const int64_t* __restrict__ slots, uint2* __restrict__ kc,
+                                 uint2* __restrict__ vc, int64_t num_slots, int chunks_per_row,
+                                 float k_scale, float v_scale, int* err) {
+    grid_dependency_wait();
+    allow_dependent_launch();
+    const int64_t t = blockIdx.x;
+    const int64_t s = slots[t];
+    if (s < 0) return;
+    if (s >= num_slots) {
+        if (threadIdx.x == 0) flag_error(err, PA_DEVERR_BAD_SLOT);
+        return;
+    }
+    for (int i = threadIdx.x; i < 2 * chunks_per_row; i += blockDim.x) {
+        const bool is_k = i < chunks_per_row;
+        const int c = is_k ? i : i - chunks_per_row;
+        const float sc = is_k ? k_scale : v_scale;
+        const uint4 val = __ldg((is_k ? k : v) + t * chunks_per_row + c);
+        const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = Mma<T>::unpack(w[j]);
+            q[j] = f32x2_to_e4m3x2(__fdiv_rn(f.y, sc), __fdiv_rn(f.x, sc));
+        }
+        (is_k ? kc : vc)[s * chunks_per_row + c] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+    }
+}
+
+cudaError_t launch_reshape_and_cache_fp8(int dtype, const void* k, const void* v,
+                                         const int64_t* slots, void* kc, void* vc,
+                                         int64_t num_tokens, int64_t num_slots, int row_elems,
+                                         float k_scale, float v_scale, int* err,
+                                         cudaStream_t stream) {
+    const int chunks = row_elems / 8;
+    const int threads = 2 * chunks < 256 ? ((2 * chunks + 31) / 32) * 32 : 256;
+    const dim3 grid((unsigned)num_tokens);
+    if (dtype == PA_BF16)
+        return launch_with_pdl(reshape_and_cache_fp8_kernel<__nv_bfloat16>, grid, dim3(threads), 0,
+                               stream, static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                               slots, static_cast<uint2*>(kc), static_cast<uint2*>(vc), num_slots,
+                               chunks, k_scale, v_scale, err);
+    return launch_with_pdl(reshape_and_cache_fp8_kernel<__half>, grid, dim3(threads), 0, stream,
+                           static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots,
+                           static_cast<uint2*>(kc), static_cast<uint2*>(vc), num_slots, chunks,
+                           k_scale, v_scale, err);
 }
 
 // ---------------------------------------------------------------------------

@@ -10,4 +10,9 @@ cudaError_t launch_decode_bf16(int head_dim, int mode, const CUtensorMap& tmk,
     return launch_decode_t<__nv_bfloat16, 128>(mode, tmk, tmv, p, grid, stream);
 }
 
+cudaError_t launch_decode_fp8_bf16(int mode, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+    return launch_decode_fp8_t<__nv_bfloat16>(mode, tmk, tmv, p, grid, stream);
+}
+
 }  // namespace pa

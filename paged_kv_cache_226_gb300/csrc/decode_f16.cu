@@ -15,4 +15,9 @@ int decode_merge_floats(int head_dim) {
                           : kConsumerWarps * DecodeLayout<128>::kMergeFloatsPerWarp;
 }
 
+cudaError_t launch_decode_fp8_f16(int mode, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+    return launch_decode_fp8_t<__half>(mode, tmk, tmv, p, grid, stream);
+}
+
 }  // namespace pa

@@ -35,40 +35,87 @@ namespace pa {
 // Rescale the accumulator only when the max grows by more than 2^8.
 constexpr float kRescaleThresholdLog2 = 8.0f;
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct DecodeLayout {
-    static constexpr int kHalves = D / kBoxElems;                 // boxes per tile
-    static constexpr int kBoxBytes = kTileTokens * kBoxElems * 2; // 2 KB
-    static constexpr int kTileBytes = kHalves * kBoxBytes;        // one of K or V
-    static constexpr int kStageBytes = 2 * kTileBytes;            // K and V
-    static constexpr int kPipeBytes = kStages * kStageBytes;
+    static constexpr int kRing = kFp8 ? kStagesFp8 : kStages;     // tiles in flight per CTA
+    // TMA-staged tiles: 16 tokens x (64 dims x 2 B | 128 dims x 1 B) per box
+    static constexpr int kHalves = kFp8 ? 1 : D / kBoxElems;      // boxes per staged tile
+    static constexpr int kBoxBytes = kTileTokens * 128;            // 2 KB
+    static constexpr int kTileBytes = kHalves * kBoxBytes;         // one of K or V
+    static constexpr int kStageBytes = 2 * kTileBytes;             // K and V
+    static constexpr int kPipeBytes = kRing * kStageBytes;
+    // 16-bit compute tiles (the layout ldmatrix reads): D/64 boxes of [16][128 B]
+    static constexpr int kHalves16 = D / kBoxElems;
+    static constexpr int kTile16Bytes = kHalves16 * kBoxBytes;
+    // FP8: each consumer warp converts its staged tile into private K and V tiles
+    static constexpr int kConvBytes = kFp8 ? kConsumerWarps * 2 * kTile16Bytes : 0;
     // merge area: per warp, O[8][D] then m_used[8], l[8], m_true[8]
     static constexpr int kMergeFloatsPerWarp = kMaxGroup * D + 3 * kMaxGroup;
     static constexpr int kMergeBytes = kConsumerWarps * kMergeFloatsPerWarp * 4;
-    static constexpr int kBodyBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+    static constexpr int kBodyBytes = (kPipeBytes + kConvBytes) > kMergeBytes
+                                          ? (kPipeBytes + kConvBytes) : kMergeBytes;
     static constexpr int kDynamicSmem = kBodyBytes + 1024;         // + alignment slack
 };
 
-template <typename T, int D, int kMode>
-__global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
+// The fused step's new token, 16-byte chunk c (8 dims) of its K (is_k) or V
+// row for KV head g: written to the cache at new_slot and returned in the
+// 16-bit compute type.  With an FP8 cache the chunk is quantised first
+// (E4M3 of x / scale, the quotient in fp32) and the returned values are the
+// codes' values -- what attention reads back from the cache.
+template <typename T, int D, bool kFp8>
+__device__ __forceinline__ uint4 new_token_chunk(const DecodeParams& p, int b, int g,
+                                                 int64_t new_slot, int c, bool is_k) {
+    const size_t row = ((size_t)b * p.num_kv_heads + g) * D;
+    const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                                reinterpret_cast<const T*>(is_k ? p.k_new : p.v_new) + row) + c);
+    const size_t dst = ((size_t)new_slot * p.num_kv_heads + g) * D;
+    if (!kFp8) {
+        T* cache = reinterpret_cast<T*>(is_k ? p.k_cache : p.v_cache);
+        reinterpret_cast<uint4*>(cache + dst)[c] = val;
+        return val;
+    }
+    const float sc = is_k ? p.k_scale : p.v_scale;
+    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+    uint16_t q[4];
+    uint32_t back[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = Mma<T>::unpack(w[j]);
+        q[j] = f32x2_to_e4m3x2(__fdiv_rn(f.y, sc), __fdiv_rn(f.x, sc));
+        back[j] = e4m3x2_to<T>(q[j]);
+    }
+    uint8_t* cache = reinterpret_cast<uint8_t*>(is_k ? p.k_cache : p.v_cache);
+    *reinterpret_cast<uint2*>(cache + dst + 8 * c) =
+        make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+    return make_uint4(back[0], back[1], back[2], back[3]);
+}
+
+template <typename T, int D, int kMode, bool kFp8 = false>
+__global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMinCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
                         const __grid_constant__ DecodeParams p) {
-    using Lay = DecodeLayout<D>;
+    using Lay = DecodeLayout<D, kFp8>;
     using M = Mma<T>;
+    static_assert(!kFp8 || D == 128, "the FP8 cache is built for head_dim 128");
     constexpr int kKSteps = D / 16;     // 16-dim slices of D
     constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
 
     constexpr bool kPartitioned = kMode != kModeSingle;
-    __shared__ __align__(8) uint64_t full_bar[kStages];
-    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t full_bar[Lay::kRing];
+    __shared__ __align__(8) uint64_t empty_bar[Lay::kRing];
     __shared__ int merge_here;          // fused step: this CTA merges the partitions
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
+    // Grid (sequences, KV heads, partitions): sequences vary fastest, so CTAs
+    // launch partition by partition -- every first partition, then every
+    // second one, ...; the later, shorter last partitions of long sequences
+    // come at the end, which keeps the tail of the grid short.
+    const int b = blockIdx.x;
     const int g = blockIdx.y;
-    const int b = blockIdx.z;
+    const int part = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = p.group;
@@ -80,14 +127,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     const int max_ctx = p.max_blocks_per_seq * p.block_size;
     int L = p.context_lens[b];
     if (L < 0 || L > max_ctx) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+        if (threadIdx.x == 0 && part == 0 && g == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
         L = L < 0 ? 0 : max_ctx;
     }
     int t_begin = 0, t_end = L, parts = 1;
     if (kPartitioned) {
         parts = min((L + p.partition_tokens - 1) / p.partition_tokens, p.max_parts);
-        t_begin = blockIdx.x * p.partition_tokens;
-        if (kMode == kModeStep && L == 0 && blockIdx.x == 0) {
+        t_begin = part * p.partition_tokens;
+        if (kMode == kModeStep && L == 0 && part == 0) {
             // Empty context: zero output; a new token cannot belong to it.
             T* out = reinterpret_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)g * G) * D;
             for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = from_float<T>(0.f);
@@ -107,7 +154,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     const int n_tiles = (t_end + kTileTokens - 1) / kTileTokens - tile_begin;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < Lay::kRing; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
@@ -138,8 +185,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
                 const int pblk = __shfl_sync(0xffffffffu, blk, k);
                 if (lane == 0) {
                     const int it = i0 + k;
-                    const int st = it % kStages;
-                    if (it >= kStages && !mbar_wait(&empty_bar[st], ((it / kStages) - 1) & 1)) {
+                    const int st = it % Lay::kRing;
+                    if (it >= Lay::kRing && !mbar_wait(&empty_bar[st], ((it / Lay::kRing) - 1) & 1)) {
                         flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
                         ok = false;
                     } else {
@@ -211,7 +258,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     // them into the staged tile in place of what the TMA read there.
     int64_t new_slot = -1;
     int new_tile = -1;                      // CTA-local tile index, -1: not attended here
-    if (kMode == kModeStep && blockIdx.x == parts - 1) {
+    if (kMode == kModeStep && part == parts - 1) {
         const int64_t slot = p.slot_mapping[b];
         if (slot >= 0) {
             const int pos = L - 1;
@@ -227,31 +274,56 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     }
 
     for (int it = warp; it < n_tiles; it += kConsumerWarps) {
-        const int st = it % kStages;
-        bool ok = mbar_wait(&full_bar[st], (it / kStages) & 1);
+        const int st = it % Lay::kRing;
+        bool ok = mbar_wait(&full_bar[st], (it / Lay::kRing) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
             break;
         }
         uint8_t* ktile = smem + st * Lay::kStageBytes;
         uint8_t* vtile = ktile + Lay::kTileBytes;
+        if (kFp8) {
+            // E4M3 -> T into this warp's private tiles, then free the stage.
+            // Unit u: K/V = u >> 7, row r, 16-byte source chunk c (dims 16c..16c+15).
+            uint8_t* conv = smem + Lay::kPipeBytes + warp * 2 * Lay::kTile16Bytes;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int u = lane + 32 * i;
+                const int kv = u >> 7, r = (u >> 3) & 15, c = u & 7;
+                const uint4 raw = *reinterpret_cast<const uint4*>(
+                    ktile + kv * Lay::kTileBytes + r * 128 + ((c ^ (r & 7)) << 4));
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                uint32_t h[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    h[2 * j] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] & 0xffffu));
+                    h[2 * j + 1] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] >> 16));
+                }
+                uint8_t* dst = conv + kv * Lay::kTile16Bytes + (c >> 2) * Lay::kBoxBytes + r * 128;
+                const int j0 = 2 * (c & 3);
+                *reinterpret_cast<uint4*>(dst + ((j0 ^ (r & 7)) << 4)) =
+                    make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4*>(dst + (((j0 + 1) ^ (r & 7)) << 4)) =
+                    make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[st]);
+            ktile = conv;
+            vtile = conv + Lay::kTile16Bytes;
+        }
         const uint32_t kbase = smem_u32(ktile);
         const uint32_t vbase = smem_u32(vtile);
 
         if (kMode == kModeStep && it == new_tile) {
-            // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V
+            // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V (in the 16-bit tile)
             const int r = (L - 1) % kTileTokens;
             const int c = lane & 15;
             if (c < D / 8) {
                 const bool is_k = lane < 16;
-                const size_t row = ((size_t)b * p.num_kv_heads + g) * D;
-                const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                                            reinterpret_cast<const T*>(is_k ? p.k_new : p.v_new) + row) + c);
+                const uint4 val = new_token_chunk<T, D, kFp8>(p, b, g, new_slot, c, is_k);
                 uint8_t* tile = is_k ? ktile : vtile;
                 *reinterpret_cast<uint4*>(tile + (c >> 3) * Lay::kBoxBytes + r * 128 +
                                           (((c & 7) ^ (r & 7)) << 4)) = val;
-                T* cache = reinterpret_cast<T*>(is_k ? p.k_cache : p.v_cache);
-                reinterpret_cast<uint4*>(cache + ((size_t)new_slot * p.num_kv_heads + g) * D)[c] = val;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -328,7 +400,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
         if (tok0 + kTileTokens > t_end) {
             const int valid = t_end - tok0;
             const int rows = kTileTokens - valid;
-            for (int idx = lane; idx < Lay::kHalves * rows * 8; idx += 32) {
+            for (int idx = lane; idx < Lay::kHalves16 * rows * 8; idx += 32) {
                 const int hh = idx / (rows * 8);
                 const int rem = idx - hh * rows * 8;
                 const int rr = valid + (rem >> 3);
@@ -351,19 +423,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
             if (kSplitP) M::run(acc[n], a0, a1, a2, a3, pl0, pl1);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[st]);
+        if (!kFp8 && lane == 0) mbar_arrive(&empty_bar[st]);
     }
 
     if (kMode == kModeStep && new_slot >= 0 && new_tile < 0 && warp == 0) {
         const int c = lane & 15;
-        if (c < D / 8) {
-            const bool is_k = lane < 16;
-            const size_t row = ((size_t)b * p.num_kv_heads + g) * D;
-            const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                                        reinterpret_cast<const T*>(is_k ? p.k_new : p.v_new) + row) + c);
-            T* cache = reinterpret_cast<T*>(is_k ? p.k_cache : p.v_cache);
-            reinterpret_cast<uint4*>(cache + ((size_t)new_slot * p.num_kv_heads + g) * D)[c] = val;
-        }
+        if (c < D / 8) (void)new_token_chunk<T, D, kFp8>(p, b, g, new_slot, c, lane < 16);
     }
 
     // row sums across the 8 lanes that share a head pair
@@ -430,10 +495,10 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
             o3 += f * v.w;
             mt = fmaxf(mt, wo[kMaxGroup * D + 2 * kMaxGroup + h]);
         }
-        const float inv = 1.f / den;
+        const float inv = (kFp8 ? p.v_scale : 1.f) / den;
         const size_t qh = (size_t)b * p.num_q_heads + (size_t)g * G + h;
         if (kMode == kModeSplit || (kMode == kModeStep && parts > 1)) {
-            const size_t idx = qh * p.max_parts + blockIdx.x;
+            const size_t idx = qh * p.max_parts + part;
             *reinterpret_cast<float4*>(p.tmp_out + idx * D + d) =
                 make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
             if (d == 0) {
@@ -522,14 +587,14 @@ __global__ void __launch_bounds__(kDecodeThreads, kMinCtasPerSm)
     }
 }
 
-template <typename T, int D, int kMode>
+template <typename T, int D, int kMode, bool kFp8 = false>
 cudaError_t launch_decode_mode(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-    const int smem = DecodeLayout<D>::kDynamicSmem;
-    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, kMode>,
+    const int smem = DecodeLayout<D, kFp8>::kDynamicSmem;
+    cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, kMode, kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_with_pdl(paged_decode_kernel<T, D, kMode>, grid, dim3(kDecodeThreads), smem,
+    e = launch_with_pdl(paged_decode_kernel<T, D, kMode, kFp8>, grid, dim3(kDecodeThreads), smem,
                         stream, tmk, tmv, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -541,6 +606,16 @@ cudaError_t launch_decode_t(int mode, const CUtensorMap& tmk, const CUtensorMap&
     if (mode == kModeSplit) return launch_decode_mode<T, D, kModeSplit>(tmk, tmv, p, grid, stream);
     if (mode == kModeStep) return launch_decode_mode<T, D, kModeStep>(tmk, tmv, p, grid, stream);
     return launch_decode_mode<T, D, kModeSingle>(tmk, tmv, p, grid, stream);
+}
+
+template <typename T>
+cudaError_t launch_decode_fp8_t(int mode, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+    if (mode == kModeSplit)
+        return launch_decode_mode<T, 128, kModeSplit, true>(tmk, tmv, p, grid, stream);
+    if (mode == kModeStep)
+        return launch_decode_mode<T, 128, kModeStep, true>(tmk, tmv, p, grid, stream);
+    return launch_decode_mode<T, 128, kModeSingle, true>(tmk, tmv, p, grid, stream);
 }
 
 }  // namespace pa

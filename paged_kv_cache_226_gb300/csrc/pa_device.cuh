@@ -203,6 +203,38 @@ struct Mma<__nv_bfloat16> {
     }
 };
 
+// ---- FP8 (E4M3) conversions ----------------------------------------------
+
+// Two E4M3 codes (high byte -> high half) to two fp16, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+// Nearest E4M3 codes (ties to even, saturating at +-448) of two floats; hi
+// lands in the high byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t e4m3x2_to(uint16_t v);
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__half>(uint16_t v) {
+    return e4m3x2_to_f16x2(v);
+}
+template <>
+__device__ __forceinline__ uint32_t e4m3x2_to<__nv_bfloat16>(uint16_t v) {
+    // E4M3 values are exact in fp16, fp32 and bf16 alike
+    uint32_t h = e4m3x2_to_f16x2(v);
+    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+    __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
 // 2^x through the hardware's ex2.approx (x = -inf gives +0).
 __device__ __forceinline__ float ex2(float x) {
     float y;

@@ -29,6 +29,11 @@ constexpr int kMinCtasPerSm = PA_DECODE_MIN_CTAS_PER_SM;
 // one warp, which waits on its phases in order; otherwise two warps would
 // share a stage and a parity wait could match a phase two laps old.
 static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
+// The FP8 cache halves the bytes of a tile, so its ring is twice as deep
+// (and the CTA keeps a 16-bit copy per warp): 4 CTAs per SM.
+constexpr int kStagesFp8 = 2 * kStages;
+constexpr int kMinCtasPerSmFp8 = 4;
+static_assert(kStagesFp8 % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
 constexpr int kMaxGroup = 8;         // query heads per KV head served by one CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -58,6 +63,9 @@ struct DecodeParams {
     void* v_cache;
     int* counters;                 // [B][Hkv] arrivals per (sequence, KV head), 0 on entry
     int num_kv_heads;
+    // FP8 (E4M3) cache only: per-tensor scales (k_scale is also folded into scale_log2)
+    float k_scale;
+    float v_scale;
 };
 
 // Decode kernel modes.
@@ -82,6 +90,15 @@ struct ReduceParams {
 cudaError_t launch_decode(int dtype, int head_dim, int mode, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
                           cudaStream_t stream);
+// Same over an FP8 (E4M3) cache; head_dim 128 only.
+cudaError_t launch_decode_fp8(int dtype, int mode, const CUtensorMap& tmk,
+                              const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
+                              cudaStream_t stream);
+cudaError_t launch_reshape_and_cache_fp8(int dtype, const void* k, const void* v,
+                                         const int64_t* slots, void* kc, void* vc,
+                                         int64_t num_tokens, int64_t num_slots, int row_elems,
+                                         float k_scale, float v_scale, int* err,
+                                         cudaStream_t stream);
 // Float capacity of the decode kernel's merge area (bounds G * S in the fused step).
 int decode_merge_floats(int head_dim);
 cudaError_t launch_reduce(int dtype, int head_dim, const ReduceParams& p, int num_seqs,

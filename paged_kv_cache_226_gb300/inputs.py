@@ -401,6 +401,13 @@ def build_workload(name: Optional[str] = None, seed: Optional[int] = None,
                           (pool.ref_count[shared[0]] if shared else 0)})
 
 
+def fp8_codes(rng: np.random.Generator, shape, scale: float) -> torch.Tensor:
+    """uint8 E4M3 codes of N(0,1) / scale (clipped to +-448), for a synthetic
+    FP8 cache whose elements are code values times ``scale``."""
+    x = normal_tensor(rng, shape, "bf16").float() / scale
+    return x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """Raw uint16 bit patterns of a CPU fp16/bf16 tensor (no copy)."""
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -65,6 +65,14 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pa_split_workspace_size.restype = ctypes.c_size_t
         lib.pa_decode_split.argtypes = [V, V, V, V, V, F, I32, I32, V, V, V, S, V]
         lib.pa_reduce.argtypes = [V, V, V, V, I32, I32, V, S, V]
+        lib.pa_reshape_and_cache_fp8.argtypes = [V, V, V, V, V, I64, F, F, S, V]
+        lib.pa_decode_fp8.argtypes = [V, V, V, V, V, F, F, F, V, S, V]
+        lib.pa_decode_split_fp8.argtypes = [V, V, V, V, V, F, F, F, I32, I32, V, V, V, S, V]
+        lib.pa_decode_step_fp8.argtypes = [V, V, V, V, V, V, V, V, F, F, F, I32, I32, V, V, V, V,
+                                           V, S, V]
+        for fn in ("pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_split_fp8",
+                   "pa_decode_step_fp8"):
+            getattr(lib, fn).restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [V, V, I64, V, V, I64, V, I64, S, V]
         lib.pa_copy_blocks.restype = ctypes.c_int
         lib.pa_decode_step.argtypes = [V, V, V, V, V, V, V, V, F, I32, I32, V, V, V, V, V, S, V]
@@ -232,13 +240,18 @@ def reduce(tmp_out, max_logits, exp_sums, context_lens, partition_size: int,
     """Log-sum-exp merge of decode_split's partitions into out [B][Hq][D]."""
     lib = load()
     dev = out.device
-    _need(out, "out", k_cache.dtype, dev)
+    _need(out, "out", out.dtype, dev)
     for t, n in ((tmp_out, "tmp_out"), (max_logits, "max_logits"), (exp_sums, "exp_sums")):
         _need(t, n, torch.float32, dev)
     _need(context_lens, "context_lens", torch.int32, dev)
     B, hq, d = out.shape
     S = tmp_out.shape[2]
-    shp = make_shape(B, hq, k_cache, max_blocks_per_seq)
+    if k_cache.dtype == torch.uint8:                     # FP8 cache: out keeps its own type
+        shp = _fp8_shape(B, hq, k_cache, max_blocks_per_seq, out.dtype)
+    else:
+        if out.dtype != k_cache.dtype:
+            raise TypeError("out must have the cache's dtype")
+        shp = make_shape(B, hq, k_cache, max_blocks_per_seq)
     _check("pa_reduce", lib.pa_reduce(_ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums),
                                       _ptr(context_lens), int(partition_size), int(S), _ptr(out),
                                       ctypes.byref(shp), _stream_handle(dev)))
@@ -298,6 +311,113 @@ def copy_blocks(k_src: torch.Tensor, v_src: torch.Tensor, k_dst: torch.Tensor,
                lib.pa_copy_blocks(_ptr(k_src), _ptr(v_src), k_src.shape[0], _ptr(k_dst),
                                   _ptr(v_dst), k_dst.shape[0], _ptr(mp), mp.shape[0],
                                   ctypes.byref(shp), _stream_handle(dev)))
+
+
+# ---- FP8 (E4M3) KV cache ---------------------------------------------------
+#
+# The cache tensors are torch.uint8 [num_blocks][block_size][Hkv][D] holding
+# E4M3 codes; element value = e4m3(code) * scale, one scale for K and one for V.
+# q, the new tokens and the output keep their fp16 / bf16 type.
+
+def _fp8_shape(num_seqs, num_q_heads, k_cache: torch.Tensor, max_blocks_per_seq, dtype):
+    nb, bs, hkv, d = k_cache.shape
+    if k_cache.dtype != torch.uint8:
+        raise TypeError("an FP8 cache is a torch.uint8 tensor of E4M3 codes")
+    return PaShape(num_seqs=num_seqs, num_q_heads=num_q_heads, num_kv_heads=hkv, head_dim=d,
+                   block_size=bs, max_blocks_per_seq=max_blocks_per_seq, num_blocks=nb,
+                   dtype=_DTYPE_CODES[dtype], reserved=0)
+
+
+def reshape_and_cache_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale: float,
+                          v_scale: float) -> None:
+    """Quantise each new token's K/V to E4M3 (x / scale) into its cache slot."""
+    lib = load()
+    dev = k_cache.device
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8, dev)
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t, n, k.dtype, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    T = slot_mapping.shape[0]
+    if k.shape != (T, k_cache.shape[2], k_cache.shape[3]) or v.shape != k.shape:
+        raise ValueError("k and v must be [num_tokens][num_kv_heads][head_dim]")
+    shp = _fp8_shape(0, k_cache.shape[2], k_cache, 1, k.dtype)
+    _check("pa_reshape_and_cache_fp8",
+           lib.pa_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache),
+                                        _ptr(v_cache), T, float(k_scale), float(v_scale),
+                                        ctypes.byref(shp), _stream_handle(dev)))
+
+
+def _fp8_common(q, k_cache, v_cache, block_tables, context_lens):
+    dev = k_cache.device
+    _need(q, "q", q.dtype, dev)
+    _need(k_cache, "k_cache", torch.uint8, dev)
+    _need(v_cache, "v_cache", torch.uint8, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    if q.dtype not in _DTYPE_CODES:
+        raise TypeError("q must be float16 or bfloat16")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [num_blocks][block_size][num_kv_heads][head_dim]")
+    B, hq, d = q.shape
+    if d != k_cache.shape[3] or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("inconsistent q / block_tables / context_lens shapes")
+    return _fp8_shape(B, hq, k_cache, block_tables.shape[1], q.dtype), dev
+
+
+def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float, k_scale: float,
+               v_scale: float, out=None) -> torch.Tensor:
+    """Single-pass paged decode over an E4M3 cache."""
+    lib = load()
+    shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens)
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", q.dtype, dev)
+    _check("pa_decode_fp8",
+           lib.pa_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                             _ptr(context_lens), float(scale), float(k_scale), float(v_scale),
+                             _ptr(out), ctypes.byref(shp), _stream_handle(dev)))
+    return out
+
+
+def decode_split_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                     k_scale: float, v_scale: float, partition_size: int,
+                     max_num_partitions: int, workspace=None):
+    """Per-partition outputs over an E4M3 cache (merge them with ``reduce``)."""
+    lib = load()
+    shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens)
+    tmp, ml, es = workspace if workspace is not None else split_workspace(q, max_num_partitions)
+    _check("pa_decode_split_fp8",
+           lib.pa_decode_split_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                   _ptr(context_lens), float(scale), float(k_scale),
+                                   float(v_scale), int(partition_size), int(max_num_partitions),
+                                   _ptr(tmp), _ptr(ml), _ptr(es), ctypes.byref(shp),
+                                   _stream_handle(dev)))
+    return tmp, ml, es
+
+
+def decode_step_fp8(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                    context_lens, scale: float, k_scale: float, v_scale: float,
+                    max_context_len: int, out=None, partition_size: int = DEFAULT_PARTITION,
+                    workspace=None) -> torch.Tensor:
+    """Fused decode layer-step over an E4M3 cache (pa_decode_step_fp8)."""
+    lib = load()
+    shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, q.dtype, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    out = torch.empty_like(q) if out is None else out
+    S = num_partitions(max_context_len, partition_size)
+    if workspace is None:
+        workspace = step_workspace(q, k_cache.shape[2], S)
+    tmp, ml, es, counters = workspace
+    _check("pa_decode_step_fp8",
+           lib.pa_decode_step_fp8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                  _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                  _ptr(context_lens), float(scale), float(k_scale),
+                                  float(v_scale), int(partition_size), int(S), _ptr(tmp),
+                                  _ptr(ml), _ptr(es), _ptr(counters), _ptr(out),
+                                  ctypes.byref(shp), _stream_handle(dev)))
+    return out
 
 
 def step_workspace(q: torch.Tensor, num_kv_heads: int, max_num_partitions: int):
@@ -426,11 +546,20 @@ class StepPlan:
 
     def __init__(self, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
                  context_lens, scale: float, max_context_len: int, out=None,
-                 mode: str = "auto", partition_size: int = DEFAULT_PARTITION, workspace=None):
+                 mode: str = "auto", partition_size: int = DEFAULT_PARTITION, workspace=None,
+                 k_scale: Optional[float] = None, v_scale: Optional[float] = None):
         self._lib = load()
-        shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+        self.fp8 = k_cache.dtype == torch.uint8
+        if self.fp8:
+            if k_scale is None or v_scale is None:
+                raise ValueError("an FP8 cache needs k_scale and v_scale")
+            if mode not in ("auto", "fused"):
+                raise ValueError("StepPlan runs an FP8 cache through the fused step only")
+            shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens)
+        else:
+            shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
         for t, n in ((k_new, "k_new"), (v_new, "v_new")):
-            _need(t, n, k_cache.dtype, dev)
+            _need(t, n, q.dtype, dev)
         _need(slot_mapping, "slot_mapping", torch.int64, dev)
         T = slot_mapping.shape[0]
         if k_new.shape != (T, k_cache.shape[2], k_cache.shape[3]) or v_new.shape != k_new.shape:
@@ -462,9 +591,10 @@ class StepPlan:
             tmp, ml, es, counters = workspace
             self.workspace = workspace
             self._keep += list(workspace)
+            scales = (ctypes.c_float(k_scale), ctypes.c_float(v_scale)) if self.fp8 else ()
             self._step_args = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
                                _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                               _ptr(context_lens), ctypes.c_float(scale),
+                               _ptr(context_lens), ctypes.c_float(scale), *scales,
                                ctypes.c_int32(self.partition_size),
                                ctypes.c_int32(self.num_partitions), _ptr(tmp), _ptr(ml),
                                _ptr(es), _ptr(counters), _ptr(self.out), sref)
@@ -498,7 +628,10 @@ class StepPlan:
                self._lib.pa_reshape_and_cache(*self._reshape_args, self._stream()))
 
     def decode(self):
-        if self.mode == "fused":
+        if self.mode == "fused" and self.fp8:
+            _check("pa_decode_step_fp8",
+                   self._lib.pa_decode_step_fp8(*self._step_args, self._stream()))
+        elif self.mode == "fused":
             _check("pa_decode_step", self._lib.pa_decode_step(*self._step_args, self._stream()))
         elif self.mode == "single":
             _check("pa_decode", self._lib.pa_decode(*self._decode_args, self._stream()))

@@ -427,3 +427,87 @@ def test_pins_fail_on_planted_mistake(name):
         with oracle.use_library(path):
             assert not _pins_pass(), f"pins did not catch planted mistake {name}"
     assert _pins_pass()
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) KV cache: decoding, quantisation, and attention over it
+# --------------------------------------------------------------------------
+
+def _torch_e4m3_values(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(codes.astype(np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def test_e4m3_every_code_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = np.array([oracle.e4m3_to_f64(c) for c in codes])
+    want = _torch_e4m3_values(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert oracle.e4m3_to_f64(0x7e) == 448.0 and np.isnan(oracle.e4m3_to_f64(0x7f))
+
+
+def test_e4m3_rounding_matches_torch_in_range():
+    rng = np.random.default_rng(5)
+    ys = np.concatenate([rng.standard_normal(2000).astype(np.float32) * s
+                         for s in (0.01, 1.0, 30.0, 200.0)])
+    # exact midpoints between neighbouring codes exercise ties-to-even
+    vals = _torch_e4m3_values(np.arange(0, 0x7e, dtype=np.uint8))
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    ys = np.concatenate([ys, mids, -mids])
+    ys = ys[np.abs(ys) < 448]
+    got = np.array([oracle.f32_to_e4m3(y) for y in ys], dtype=np.uint8)
+    want = torch.from_numpy(ys).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+
+
+def test_e4m3_saturates_and_keeps_nan():
+    assert oracle.f32_to_e4m3(448.0) == 0x7e and oracle.f32_to_e4m3(1e30) == 0x7e
+    assert oracle.f32_to_e4m3(-500.0) == 0xfe and oracle.f32_to_e4m3(float("-inf")) == 0xfe
+    assert oracle.f32_to_e4m3(float("nan")) == 0x7f
+    assert oracle.f32_to_e4m3(-0.0) == 0x80 and oracle.f32_to_e4m3(0.0) == 0x00
+
+
+def test_fp8_cache_write_quantises_x_over_scale():
+    w = _small_workload("bf16", hq=8, hkv=2, d=64, lens=(3, 20, 33))
+    kc0 = np.zeros((w.num_blocks, w.block_size, 2, 64), np.uint8)
+    vc0 = np.full_like(kc0, 0x38)
+    ks, vs = 0.05, 0.11
+    kc, vc, bad = oracle.reshape_and_cache_fp8(pin.bits(w.k_new), pin.bits(w.v_new),
+                                               w.slot_mapping, kc0, vc0, w.block_size, "bf16",
+                                               ks, vs)
+    assert bad == 0
+    for src, cache, base, sc in ((w.k_new, kc, kc0, ks), (w.v_new, vc, vc0, vs)):
+        y = (src.float() / torch.tensor(sc, dtype=torch.float32)).numpy()   # fp32 quotient
+        y = np.clip(y, -448, 448)
+        codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        want = base.copy().reshape(w.num_blocks * w.block_size, -1)
+        want[w.slot_mapping] = codes.reshape(len(w.slot_mapping), -1)
+        assert np.array_equal(cache.reshape(want.shape), want)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_fp8_decode_matches_sdpa_on_dequantised_cache(dtype):
+    w = _small_workload(dtype, hq=16, hkv=4, d=128, lens=(1, 17, 48, 90))
+    rng = np.random.default_rng(11)
+    kc = rng.integers(0, 256, size=(w.num_blocks, w.block_size, 4, 128), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=kc.shape, dtype=np.uint8)
+    kc[(kc & 0x7f) == 0x7f] = 0x10                   # no NaN codes
+    vc[(vc & 0x7f) == 0x7f] = 0x21
+    ks, vs = 0.02, 0.3
+    got = oracle.paged_decode_fp8(pin.bits(w.q), kc, vc, w.block_tables, w.context_lens,
+                                  w.scale, ks, vs, dtype)
+    kf = _torch_e4m3_values(kc) * ks
+    vf = _torch_e4m3_values(vc) * vs
+    q = oracle.widen(pin.bits(w.q), dtype)
+    G = 4
+    for b in range(w.num_seqs):
+        L = int(w.context_lens[b])
+        idx = np.arange(L)
+        phys = w.block_tables[b][idx // w.block_size]
+        K = torch.from_numpy(kf[phys, idx % w.block_size]).permute(1, 0, 2).repeat_interleave(G, 0)
+        V = torch.from_numpy(vf[phys, idx % w.block_size]).permute(1, 0, 2).repeat_interleave(G, 0)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q[b]).unsqueeze(1), K, V, scale=w.scale)[:, 0].numpy()
+        np.testing.assert_allclose(got[b], o, rtol=1e-12, atol=1e-12)
