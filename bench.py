@@ -107,7 +107,7 @@ def step_bytes(w: pin.Workload, mode: str, partition: int, cache_elem_bytes: int
     parts = sum(-(-int(L) // partition) for L in w.context_lens)
     split_w = parts * hq * (d + 2) * 4                  # tmp_out + max_logits + exp_sums
     kernels = {"reshape_and_cache": new_tok + write_tok + w.num_tokens * 8}
-    if mode == "fused":
+    if mode in ("fused", "balanced"):
         kernels = {"paged_decode_step": kv + q + out + new_tok + write_tok + w.num_tokens * 8}
     elif mode == "split":
         kernels["paged_decode_split"] = kv + q + split_w
@@ -320,8 +320,8 @@ def bench_ours(args):
 
     kc, vc, scales = w.k_cache, w.v_cache, {}
     if args.kv_dtype == "fp8":
-        if mode != "fused":
-            raise SystemExit("--kv-dtype fp8 runs the fused step")
+        if mode not in ("fused", "balanced"):
+            raise SystemExit("--kv-dtype fp8 runs the fused steps")
         rng = np.random.default_rng(rank_seed(args.config, rank) + 7)
         kc = pin.fp8_codes(rng, tuple(w.k_cache.shape), FP8_K_SCALE)
         vc = pin.fp8_codes(rng, tuple(w.v_cache.shape), FP8_V_SCALE)
@@ -425,7 +425,7 @@ def bench_ours(args):
 
     hbm, peak_src = peaks()
     dom = {"split": "paged_decode_split", "single": "paged_decode",
-           "fused": "paged_decode_step"}[mode]
+           "fused": "paged_decode_step", "balanced": "paged_decode_step"}[mode]
     dom_ms = sum(k2_ms) / len(k2_ms)
     dom_bytes = nb["kernels"][dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -450,7 +450,7 @@ def bench_ours(args):
                    "kv_bytes": nb["kv"], "kv_bytes_unique": w.kv_bytes_unique() * (
                        1 if args.kv_dtype != "fp8" else 0.5),
                    "bytes_per_step": nb["layer_step"], "seqs_per_gpu": w.num_seqs},
-        "kernels_us": {**({} if mode == "fused" else
+        "kernels_us": {**({} if mode in ("fused", "balanced") else
                           {"reshape_and_cache": round(1e3 * sum(k1_ms) / len(k1_ms), 2)}),
                        dom: round(1e3 * dom_ms, 2),
                        "note": f"event-bracketed, serialised, over {n_attr} more steps; the "
@@ -462,7 +462,7 @@ def bench_ours(args):
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "traffic": profiled_traffic(args.config, dom)},
         "clocks": clk.summary(t_epoch0, t_epoch1),
-        "gpu_launches": {"split": 3, "single": 2, "fused": 1}[mode] * args.steps,
+        "gpu_launches": {"split": 3, "single": 2, "fused": 1, "balanced": 2}[mode] * args.steps,
         "device_errors": errs,
         "wall_s_timed": round(t_wall, 4),
         "e2e": e2e,
@@ -476,14 +476,70 @@ def bench_ours(args):
     return 0
 
 
+def bench_copy(args):
+    """Whole-block copies (pa_copy_blocks): copy-on-write inside the device
+    pool and swap-out to pinned host memory, over the workload's pool."""
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pa_build.build()
+    lib.load()
+    w = make_workload(args, rank)
+    rng = np.random.default_rng(5)
+    nb = w.num_blocks
+    n_pairs = min(4096, nb // 2)
+    perm = rng.permutation(nb)
+    cow = torch.from_numpy(np.stack([perm[:n_pairs], perm[n_pairs:2 * n_pairs]], 1)).to(dev)
+    kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
+    hk = torch.empty((n_pairs,) + tuple(kc.shape[1:]), dtype=kc.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    swap = torch.from_numpy(np.stack([perm[:n_pairs], np.arange(n_pairs)], 1)).to(dev)
+    block_bytes = kc[0].numel() * kc.element_size() * 2          # K and V
+    res = {}
+    for name, (src, dst, mp) in {"copy_on_write": ((kc, vc), (kc, vc), cow),
+                                 "swap_out": ((kc, vc), (hk, hv), swap),
+                                 "swap_in": ((hk, hv), (kc, vc),
+                                             torch.flip(swap, [1]).contiguous())}.items():
+        for _ in range(args.warmup):
+            lib.copy_blocks(*src, *dst, mp)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            lib.copy_blocks(*src, *dst, mp)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / args.steps
+        # bytes moved: read + write of every copied block
+        res[name] = {"us": round(ms * 1e3, 2),
+                     "GBps_rw": round(2 * n_pairs * block_bytes / (ms * 1e-3) / 1e9, 1)}
+    hbm, peak_src = peaks()
+    line = {"metric": "block copy GB/s (read + write), copy-on-write and swap",
+            "value": res["copy_on_write"]["GBps_rw"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": f"{w.name} pool, {n_pairs} block pairs of "
+                                   f"{block_bytes} bytes (K + V)"},
+            "roofline": {"bound": "hbm", "achieved": res["copy_on_write"]["GBps_rw"],
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": round(res["copy_on_write"]["GBps_rw"] / hbm, 4)},
+            "ops": res}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["step", "copy"], default="step",
+                    help="what to time: the decode layer-step, or whole-block copies")
     ap.add_argument("--config", default="llama8b", choices=sorted(pin.CONFIGS))
-    ap.add_argument("--mode", default="auto", choices=["auto", "single", "split", "fused"])
+    ap.add_argument("--mode", default="auto", choices=["auto", "single", "split", "fused",
+                                                       "balanced"])
     ap.add_argument("--partition", type=int, default=0,
                     help="tokens per partition (0: chosen from the batch shape)")
     ap.add_argument("--params", default="", help="JSON overrides of the workload parameters")
@@ -495,6 +551,8 @@ def main(argv=None):
     args.warmup = max(args.warmup, 3)        # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return bench_reference(args)
+    if args.op == "copy":
+        return bench_copy(args)
     return bench_ours(args)
 
 

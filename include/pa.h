@@ -157,6 +157,29 @@ int pa_reduce(const float* tmp_out, const float* max_logits, const float* exp_su
               int32_t max_num_partitions, void* out, const pa_shape* shp, void* stream);
 
 /*
+ * pa_decode_step_balanced: the fused layer-step of pa_decode_step (same
+ * inputs, same results) with the work balanced over one wave of CTAs instead
+ * of one CTA per context partition: the 16-token tiles of all (sequence,
+ * KV head) pairs, in order, are dealt out in equal contiguous ranges to the
+ * consumer warps of the grid; a warp's range may cover the end of one
+ * sequence and the start of the next, and pieces of one (sequence, KV head)
+ * are merged (log-sum-exp) by the warp that finishes last.  Suited to
+ * batches of many short or ragged contexts.
+ * workspace: device memory of at least pa_balanced_workspace_size(shp)
+ * bytes, 16-byte aligned, all zero before the first call (it holds
+ * per-(sequence, KV head) counters that every call leaves at zero; zero it
+ * again after a PA_DEVERR_WAIT_TIMEOUT).  Calls that overlap on the GPU must
+ * not share a workspace.  Other arguments and errors as pa_decode_step.
+ * Two launches (a one-CTA plan kernel, then the attention kernel).
+ */
+size_t pa_balanced_workspace_size(const pa_shape* shp);
+int pa_decode_step_balanced(const void* q, const void* k, const void* v,
+                            const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens, float scale,
+                            void* workspace, size_t workspace_bytes, void* out,
+                            const pa_shape* shp, void* stream);
+
+/*
  * FP8 KV cache.  The pages name the KV-cache data type as a knob that, like
  * weight quantisation, shrinks the KV pool so that more requests fit
  * (ta-paperlens page, --quantization / --kv-cache-dtype; youngju.dev post,
@@ -195,6 +218,14 @@ int pa_decode_step_fp8(const void* q, const void* k, const void* v, const int64_
                        int32_t partition_size, int32_t max_num_partitions, float* tmp_out,
                        float* max_logits, float* exp_sums, int32_t* counters, void* out,
                        const pa_shape* shp, void* stream);
+
+/* pa_decode_step_balanced over an E4M3 cache. */
+int pa_decode_step_balanced_fp8(const void* q, const void* k, const void* v,
+                                const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float scale, float k_scale, float v_scale, void* workspace,
+                                size_t workspace_bytes, void* out, const pa_shape* shp,
+                                void* stream);
 
 /*
  * pa_copy_blocks: copy whole physical blocks between two block pools.  For

@@ -331,9 +331,139 @@ int decode_step(const void* q, const void* k, const void* v, const int64_t* slot
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+// Consumer warps of the balanced step's grid on the current device (one wave:
+// every SM holds the 16-bit kernel's resident CTAs; the FP8 grid uses fewer).
+cudaError_t balanced_grid(int* num_ctas, bool fp8) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    *num_ctas = sms * (fp8 ? pa::kMinCtasPerSmFp8 : pa::kMinCtasPerSm);
+    return cudaSuccess;
+}
+
+struct BalancedWorkspace {
+    int* counters;
+    int* plan;
+    float* rec_m;
+    float* rec_l;
+    float* rec_o;
+    size_t bytes;
+};
+
+// [counters B*Hkv][plan][rec_m R*G][rec_l R*G][rec_o R*G*D], each part
+// 256-byte aligned, R = max consumer warps + B*Hkv.
+BalancedWorkspace balanced_layout(const pa_shape* s, int max_warps, void* base) {
+    const size_t B = s->num_seqs, Hkv = s->num_kv_heads, G = s->num_q_heads / s->num_kv_heads;
+    const size_t R = (size_t)max_warps + B * Hkv;
+    BalancedWorkspace w{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += round256(bytes);
+        return static_cast<unsigned char*>(base) + at;
+    };
+    w.counters = reinterpret_cast<int*>(take(B * Hkv * sizeof(int)));
+    w.plan = reinterpret_cast<int*>(
+        take(((size_t)pa::plan_starts_offset((int)B) + 4 * (size_t)max_warps) * sizeof(int)));
+    w.rec_m = reinterpret_cast<float*>(take(R * G * sizeof(float)));
+    w.rec_l = reinterpret_cast<float*>(take(R * G * sizeof(float)));
+    w.rec_o = reinterpret_cast<float*>(take(R * G * s->head_dim * sizeof(float)));
+    w.bytes = off;
+    return w;
+}
+
+int decode_step_balanced(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
+                         void* k_cache, void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, float scale, void* workspace,
+                         size_t workspace_bytes, void* out, const pa_shape* shp, void* stream,
+                         const CacheKind& ck) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if ((st = check_kind(shp, ck)) != PA_OK) return st;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !out || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    if ((int64_t)shp->num_seqs * shp->num_kv_heads * shp->max_blocks_per_seq *
+            (shp->block_size / pa::kTileTokens) >= (1ll << 31))
+        return PA_ERR_UNSUPPORTED;
+    if (!workspace || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+    int num_ctas = 0, max_ctas = 0;
+    cudaError_t e = balanced_grid(&num_ctas, ck.fp8);
+    if (e == cudaSuccess) e = balanced_grid(&max_ctas, false);
+    if (e != cudaSuccess) return cuda_fail(e);
+    BalancedWorkspace w = balanced_layout(shp, max_ctas * pa::kConsumerWarps, workspace);
+    if (w.bytes > workspace_bytes) return PA_ERR_WORKSPACE;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp, ck.fp8)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp, ck.fp8)) != PA_OK) return st;
+    int* err = nullptr;
+    e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::BalancedParams p{};
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = out;
+    p.err = err;
+    p.scale_log2 = scale * ck.k_scale * pa::kLog2e;
+    p.num_q_heads = shp->num_q_heads;
+    p.group = shp->num_q_heads / shp->num_kv_heads;
+    p.max_blocks_per_seq = shp->max_blocks_per_seq;
+    p.block_size = shp->block_size;
+    p.num_blocks = shp->num_blocks;
+    p.k_new = k;
+    p.v_new = v;
+    p.slot_mapping = slot_mapping;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.counters = w.counters;
+    p.num_kv_heads = shp->num_kv_heads;
+    p.k_scale = ck.k_scale;
+    p.v_scale = ck.v_scale;
+    p.num_seqs = shp->num_seqs;
+    p.num_warps = num_ctas * pa::kConsumerWarps;
+    p.plan = w.plan;
+    p.rec_o = w.rec_o;
+    p.rec_m = w.rec_m;
+    p.rec_l = w.rec_l;
+    e = pa::launch_balanced(shp->dtype, shp->head_dim, ck.fp8, tmk, tmv, p, num_ctas,
+                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t pa_balanced_workspace_size(const pa_shape* shp) {
+    if (check_shape(shp, true) != PA_OK) return 0;
+    int max_ctas = 0;
+    if (balanced_grid(&max_ctas, false) != cudaSuccess) return 0;
+    return balanced_layout(shp, max_ctas * pa::kConsumerWarps, nullptr).bytes;
+}
+
+int pa_decode_step_balanced(const void* q, const void* k, const void* v,
+                            const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens, float scale,
+                            void* workspace, size_t workspace_bytes, void* out,
+                            const pa_shape* shp, void* stream) {
+    return decode_step_balanced(q, k, v, slot_mapping, k_cache, v_cache, block_tables,
+                                context_lens, scale, workspace, workspace_bytes, out, shp, stream,
+                                kCache16);
+}
+
+int pa_decode_step_balanced_fp8(const void* q, const void* k, const void* v,
+                                const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                float scale, float k_scale, float v_scale, void* workspace,
+                                size_t workspace_bytes, void* out, const pa_shape* shp,
+                                void* stream) {
+    return decode_step_balanced(q, k, v, slot_mapping, k_cache, v_cache, block_tables,
+                                context_lens, scale, workspace, workspace_bytes, out, shp, stream,
+                                CacheKind{true, k_scale, v_scale});
+}
 
 int pa_decode(const void* q, const void* k_cache, const void* v_cache,
               const int32_t* block_tables, const int32_t* context_lens, float scale,

@@ -26,14 +26,9 @@
 // The four warps' (m, l, O) are merged through shared memory at the end.
 #pragma once
 
-#include <type_traits>
-
-#include "pa_device.cuh"
+#include "decode_tile.cuh"
 
 namespace pa {
-
-// Rescale the accumulator only when the max grows by more than 2^8.
-constexpr float kRescaleThresholdLog2 = 8.0f;
 
 template <int D, bool kFp8 = false>
 struct DecodeLayout {
@@ -99,7 +94,6 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
     using M = Mma<T>;
     static_assert(!kFp8 || D == 128, "the FP8 cache is built for head_dim 128");
     constexpr int kKSteps = D / 16;     // 16-dim slices of D
-    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
 
     constexpr bool kPartitioned = kMode != kModeSingle;
     __shared__ __align__(8) uint64_t full_bar[Lay::kRing];
@@ -224,33 +218,11 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
     const int c4 = lane & 3;
     const int hA = 2 * c4, hB = 2 * c4 + 1;      // this thread's two heads
 
-    // q^T as the B operand: b0 = q[r8][16kk + 2c4 ..], b1 = q[r8][16kk + 8 + 2c4 ..]
     uint32_t qb[kKSteps][2];
-    {
-        const bool qrow_valid = r8 < G;
-        const T* qrow = reinterpret_cast<const T*>(p.q) +
-                        ((size_t)b * p.num_q_heads + (size_t)g * G + (qrow_valid ? r8 : 0)) * D;
-#pragma unroll
-        for (int kk = 0; kk < kKSteps; ++kk) {
-            qb[kk][0] = qrow_valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * c4)) : 0u;
-            qb[kk][1] = qrow_valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * c4)) : 0u;
-        }
-    }
-
-    float acc[kKSteps][4];      // O^T slabs of 16 dims
-#pragma unroll
-    for (int n = 0; n < kKSteps; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    float mA = -INFINITY, mB = -INFINITY;     // reference max in use (log2 units)
-    float tA = -INFINITY, tB = -INFINITY;     // true running max (log2 units)
-    float lA = 0.f, lB = 0.f;                 // this thread's share of the row sums
-
-    // ldmatrix row addresses: matrix j = lane/8 supplies row lane%8.
-    // K (A operand, no transpose): j -> (tokens 8*(j&1).., dims hi = j>>1)
-    const int k_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
-    const int k_hi = lane >> 4;
-    // V (A operand of V^T, transposed): j -> (tokens 8*(j>>1).., dims hi = j&1)
-    const int v_tok = (lane >> 4) * 8 + (lane & 7);
-    const int v_hi = (lane >> 3) & 1;
+    load_q_fragments<T, D>(qb, reinterpret_cast<const T*>(p.q) +
+                                   ((size_t)b * p.num_q_heads + (size_t)g * G) * D, G, lane);
+    TileState<D> ts;
+    ts.reset();
 
     // Fused step: the CTA of the last partition owns the sequence's new token
     // (position L - 1).  It checks that slot_mapping[b] is that position's
@@ -283,145 +255,29 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         uint8_t* ktile = smem + st * Lay::kStageBytes;
         uint8_t* vtile = ktile + Lay::kTileBytes;
         if (kFp8) {
-            // E4M3 -> T into this warp's private tiles, then free the stage.
-            // Unit u: K/V = u >> 7, row r, 16-byte source chunk c (dims 16c..16c+15).
+            // E4M3 -> T into this warp's private tiles, then free the stage
             uint8_t* conv = smem + Lay::kPipeBytes + warp * 2 * Lay::kTile16Bytes;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int u = lane + 32 * i;
-                const int kv = u >> 7, r = (u >> 3) & 15, c = u & 7;
-                const uint4 raw = *reinterpret_cast<const uint4*>(
-                    ktile + kv * Lay::kTileBytes + r * 128 + ((c ^ (r & 7)) << 4));
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t h[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    h[2 * j] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] & 0xffffu));
-                    h[2 * j + 1] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] >> 16));
-                }
-                uint8_t* dst = conv + kv * Lay::kTile16Bytes + (c >> 2) * Lay::kBoxBytes + r * 128;
-                const int j0 = 2 * (c & 3);
-                *reinterpret_cast<uint4*>(dst + ((j0 ^ (r & 7)) << 4)) =
-                    make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(dst + (((j0 + 1) ^ (r & 7)) << 4)) =
-                    make_uint4(h[4], h[5], h[6], h[7]);
-            }
+            convert_fp8_tiles<T>(ktile, conv, conv + Lay::kTile16Bytes, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[st]);
             ktile = conv;
             vtile = conv + Lay::kTile16Bytes;
         }
-        const uint32_t kbase = smem_u32(ktile);
-        const uint32_t vbase = smem_u32(vtile);
 
         if (kMode == kModeStep && it == new_tile) {
             // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V (in the 16-bit tile)
-            const int r = (L - 1) % kTileTokens;
             const int c = lane & 15;
             if (c < D / 8) {
                 const bool is_k = lane < 16;
-                const uint4 val = new_token_chunk<T, D, kFp8>(p, b, g, new_slot, c, is_k);
-                uint8_t* tile = is_k ? ktile : vtile;
-                *reinterpret_cast<uint4*>(tile + (c >> 3) * Lay::kBoxBytes + r * 128 +
-                                          (((c & 7) ^ (r & 7)) << 4)) = val;
+                put_tile_chunk(is_k ? ktile : vtile, (L - 1) % kTileTokens, c,
+                               new_token_chunk<T, D, kFp8>(p, b, g, new_slot, c, is_k));
             }
             fence_proxy_async_smem();
             __syncwarp();
         }
 
-        // S^T for the 16 tokens of the tile
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < kKSteps; ++kk) {
-            const int chunk = 2 * kk + k_hi;                 // 16-byte chunk along D
-            const uint32_t addr = kbase + (chunk >> 3) * Lay::kBoxBytes + k_tok * 128 +
-                                  (((chunk & 7) ^ (k_tok & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(addr, a0, a1, a2, a3);
-            M::run(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-        }
-
-        // mask past the span's end, scale into log2 units
-        const int tok0 = (tile_begin + it) * kTileTokens;
-        const bool v_lo = tok0 + r8 < t_end, v_hi8 = tok0 + r8 + 8 < t_end;
-        const float x0 = v_lo ? sc[0] * p.scale_log2 : -INFINITY;    // (r8,   hA)
-        const float x1 = v_lo ? sc[1] * p.scale_log2 : -INFINITY;    // (r8,   hB)
-        const float x2 = v_hi8 ? sc[2] * p.scale_log2 : -INFINITY;   // (r8+8, hA)
-        const float x3 = v_hi8 ? sc[3] * p.scale_log2 : -INFINITY;   // (r8+8, hB)
-        float xa = fmaxf(x0, x2), xb = fmaxf(x1, x3);
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
-            xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, o));
-        }
-        tA = fmaxf(tA, xa);
-        tB = fmaxf(tB, xb);
-        const bool raiseA = xa > mA + kRescaleThresholdLog2;
-        const bool raiseB = xb > mB + kRescaleThresholdLog2;
-        if (__any_sync(0xffffffffu, raiseA || raiseB)) {
-            const float nA = raiseA ? xa : mA, nB = raiseB ? xb : mB;
-            const float fA = ex2(mA - nA), fB = ex2(mB - nB);
-#pragma unroll
-            for (int n = 0; n < kKSteps; ++n) {
-                acc[n][0] *= fA;
-                acc[n][1] *= fB;
-                acc[n][2] *= fA;
-                acc[n][3] *= fB;
-            }
-            lA *= fA;
-            lB *= fB;
-            mA = nA;
-            mB = nB;
-        }
-        // P in the cache's 16-bit type; P^T fragments by an in-register
-        // transpose.  fp16 keeps P to 2^-11; for bf16 P = hi + lo (two bf16
-        // parts, ~2^-17 together) and the product below runs once per part.
-        const float e0 = ex2(x0 - mA), e1 = ex2(x1 - mB);   // token r8
-        const float e2 = ex2(x2 - mA), e3 = ex2(x3 - mB);   // token r8+8
-        const uint32_t p01 = M::pack(e0, e1);
-        const uint32_t p23 = M::pack(e2, e3);
-        const uint32_t pb0 = movmatrix_trans(p01);   // (head r8, tokens 2c4..+1)
-        const uint32_t pb1 = movmatrix_trans(p23);   // (head r8, tokens 8+2c4..+1)
-        uint32_t pl0 = 0u, pl1 = 0u;
-        if (kSplitP) {
-            const float2 u = M::unpack(p01), w = M::unpack(p23);
-            pl0 = movmatrix_trans(M::pack(e0 - u.x, e1 - u.y));
-            pl1 = movmatrix_trans(M::pack(e2 - w.x, e3 - w.y));
-            lA += e0 + e2;
-            lB += e1 + e3;
-        } else {
-            const float2 u = M::unpack(p01), w = M::unpack(p23);
-            lA += u.x + w.x;
-            lB += u.y + w.y;
-        }
-
-        // Ragged tail: V rows past the end may hold stale non-finite bits;
-        // zero them so that 0 * V stays 0 in the product below.
-        if (tok0 + kTileTokens > t_end) {
-            const int valid = t_end - tok0;
-            const int rows = kTileTokens - valid;
-            for (int idx = lane; idx < Lay::kHalves16 * rows * 8; idx += 32) {
-                const int hh = idx / (rows * 8);
-                const int rem = idx - hh * rows * 8;
-                const int rr = valid + (rem >> 3);
-                *reinterpret_cast<uint4*>(vtile + hh * Lay::kBoxBytes + rr * 128 + ((rem & 7) << 4)) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-
-        // O^T += V^T . P^T, one m16n8k16 per 16-dim slab
-#pragma unroll
-        for (int n = 0; n < kKSteps; ++n) {
-            const int chunk = 2 * n + v_hi;
-            const uint32_t addr = vbase + (chunk >> 3) * Lay::kBoxBytes + v_tok * 128 +
-                                  (((chunk & 7) ^ (v_tok & 7)) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(addr, a0, a1, a2, a3);
-            M::run(acc[n], a0, a1, a2, a3, pb0, pb1);
-            if (kSplitP) M::run(acc[n], a0, a1, a2, a3, pl0, pl1);
-        }
+        attend_tile<T, D>(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
+                          p.scale_log2, lane);
         __syncwarp();
         if (!kFp8 && lane == 0) mbar_arrive(&empty_bar[st]);
     }
@@ -431,12 +287,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         if (c < D / 8) (void)new_token_chunk<T, D, kFp8>(p, b, g, new_slot, c, lane < 16);
     }
 
-    // row sums across the 8 lanes that share a head pair
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        lA += __shfl_xor_sync(0xffffffffu, lA, o);
-        lB += __shfl_xor_sync(0xffffffffu, lB, o);
-    }
+    ts.reduce_row_sums();
 
     // ----------------------------------------------------------------------
     // merge the consumer warps
@@ -449,24 +300,24 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         for (int n = 0; n < kKSteps; ++n) {
             const int d = 16 * n + r8;
             if (hA < G) {
-                wo[hA * D + d] = acc[n][0];
-                wo[hA * D + d + 8] = acc[n][2];
+                wo[hA * D + d] = ts.acc[n][0];
+                wo[hA * D + d + 8] = ts.acc[n][2];
             }
             if (hB < G) {
-                wo[hB * D + d] = acc[n][1];
-                wo[hB * D + d + 8] = acc[n][3];
+                wo[hB * D + d] = ts.acc[n][1];
+                wo[hB * D + d + 8] = ts.acc[n][3];
             }
         }
         if (r8 == 0) {
             if (hA < G) {
-                wo[kMaxGroup * D + hA] = mA;
-                wo[kMaxGroup * D + kMaxGroup + hA] = lA;
-                wo[kMaxGroup * D + 2 * kMaxGroup + hA] = tA;
+                wo[kMaxGroup * D + hA] = ts.mA;
+                wo[kMaxGroup * D + kMaxGroup + hA] = ts.lA;
+                wo[kMaxGroup * D + 2 * kMaxGroup + hA] = ts.tA;
             }
             if (hB < G) {
-                wo[kMaxGroup * D + hB] = mB;
-                wo[kMaxGroup * D + kMaxGroup + hB] = lB;
-                wo[kMaxGroup * D + 2 * kMaxGroup + hB] = tB;
+                wo[kMaxGroup * D + hB] = ts.mB;
+                wo[kMaxGroup * D + kMaxGroup + hB] = ts.lB;
+                wo[kMaxGroup * D + 2 * kMaxGroup + hB] = ts.tB;
             }
         }
     }

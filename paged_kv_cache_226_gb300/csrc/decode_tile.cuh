@@ -1,0 +1,217 @@
+// Per-warp attention over one 16-token tile of one (sequence, KV head), the
+// building block of every decode kernel.
+//
+// A 16-bit tile in shared memory is D/64 boxes of [16 tokens][128 B] (2 KiB
+// each) with the 128-byte swizzle TMA writes: 16-byte chunk c of row r sits
+// at chunk c ^ (r % 8).  Fragment roles (m16n8k16, r8 = lane/4, c4 = lane%4):
+//   S^T[t][h] = K[t][:] . q[h][:]        A = K tile (16 tokens x 16 dims),
+//                                        B = q^T (16 dims x 8 heads)
+//   O^T[d][h] += V^T[d][:] . P^T[:][h]   A = V^T (16 dims x 16 tokens),
+//                                        B = P^T (16 tokens x 8 heads)
+// so a lane holds scores of tokens r8 and r8+8 for heads 2c4, 2c4+1, and
+// accumulators of dims r8, r8+8 (per 16-dim slab) for the same two heads.
+// The G <= 8 query heads of the group are the 8 columns; columns >= G are
+// zero.  Online softmax in log2 units with a lazily raised running max (the
+// accumulator is rescaled only when a tile's max exceeds the max in use by
+// more than 2^8; numerator and denominator share the reference max, so the
+// result is exact in real arithmetic).  P is rounded to the 16-bit type --
+// for bf16 as a hi + lo pair (~2^-17 together) -- and transposed in
+// registers with movmatrix.
+#pragma once
+
+#include <type_traits>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kBox16Bytes = kTileTokens * 128;       // one [16][128 B] box
+constexpr float kRescaleThresholdLog2 = 8.0f;        // rescale when the max grows > 2^8
+
+template <int D>
+struct TileState {
+    float acc[D / 16][4];     // O^T slabs of 16 dims
+    float mA, mB;             // reference max in use (log2 units)
+    float tA, tB;             // true running max (log2 units)
+    float lA, lB;             // this lane's share of the row sums
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int n = 0; n < D / 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        mA = mB = tA = tB = -INFINITY;
+        lA = lB = 0.f;
+    }
+
+    // Row sums across the 8 lanes that share a head pair.
+    __device__ __forceinline__ void reduce_row_sums() {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            lA += __shfl_xor_sync(0xffffffffu, lA, o);
+            lB += __shfl_xor_sync(0xffffffffu, lB, o);
+        }
+    }
+};
+
+// q^T as the B operand: b0 = q[r8][16kk + 2c4 ..], b1 = q[r8][16kk + 8 + 2c4 ..];
+// rows >= G are zero.  q_group points at the group's first query head.
+template <typename T, int D>
+__device__ __forceinline__ void load_q_fragments(uint32_t (&qb)[D / 16][2], const T* q_group,
+                                                 int G, int lane) {
+    const int r8 = lane >> 2, c4 = lane & 3;
+    const bool valid = r8 < G;
+    const T* qrow = q_group + (valid ? r8 : 0) * D;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        qb[kk][0] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * c4)) : 0u;
+        qb[kk][1] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * c4)) : 0u;
+    }
+}
+
+// E4M3 tile pair (K then V, each one [16][128 B] box of codes for D = 128)
+// -> the 16-bit layout above; warp-cooperative, exact.
+template <typename T>
+__device__ __forceinline__ void convert_fp8_tiles(const uint8_t* src, uint8_t* dst_k,
+                                                  uint8_t* dst_v, int lane) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int u = lane + 32 * i;
+        const int kv = u >> 7, r = (u >> 3) & 15, c = u & 7;   // c: 16 dims 16c..16c+15
+        const uint4 raw = *reinterpret_cast<const uint4*>(
+            src + kv * kBox16Bytes + r * 128 + ((c ^ (r & 7)) << 4));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            h[2 * j] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] & 0xffffu));
+            h[2 * j + 1] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] >> 16));
+        }
+        uint8_t* d = (kv ? dst_v : dst_k) + (c >> 2) * kBox16Bytes + r * 128;
+        const int j0 = 2 * (c & 3);
+        // lanes of the upper half of a row store their odd chunk first, so
+        // that each store instruction of 8 lanes covers 8 distinct bank groups
+        const int first = (c >> 2) ? 1 : 0;
+        const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]), hi = make_uint4(h[4], h[5], h[6], h[7]);
+        *reinterpret_cast<uint4*>(d + (((j0 + first) ^ (r & 7)) << 4)) = first ? hi : lo;
+        *reinterpret_cast<uint4*>(d + (((j0 + 1 - first) ^ (r & 7)) << 4)) = first ? lo : hi;
+    }
+}
+
+// Writes one 16-byte chunk (8 dims) into row r of a 16-bit tile.
+__device__ __forceinline__ void put_tile_chunk(uint8_t* tile, int r, int c, uint4 val) {
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kBox16Bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+        val;
+}
+
+// Attends the 16 tokens tok0 .. tok0+15 of a tile; tokens >= t_end are masked
+// (their V rows are zeroed in shared memory, since they may hold stale
+// non-finite bits).
+template <typename T, int D>
+__device__ __forceinline__ void attend_tile(TileState<D>& s, const uint32_t (&qb)[D / 16][2],
+                                            uint8_t* ktile, uint8_t* vtile, int tok0, int t_end,
+                                            float scale_log2, int lane) {
+    using M = Mma<T>;
+    constexpr int kKSteps = D / 16;
+    constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+    const int r8 = lane >> 2;
+    // ldmatrix row addresses: matrix j = lane/8 supplies row lane%8.
+    // K (A operand, no transpose): j -> (tokens 8*(j&1).., dims hi = j>>1)
+    const int k_tok = ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int k_hi = lane >> 4;
+    // V (A operand of V^T, transposed): j -> (tokens 8*(j>>1).., dims hi = j&1)
+    const int v_tok = (lane >> 4) * 8 + (lane & 7);
+    const int v_hi = (lane >> 3) & 1;
+    const uint32_t kbase = smem_u32(ktile);
+    const uint32_t vbase = smem_u32(vtile);
+
+    // S^T for the 16 tokens of the tile
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; ++kk) {
+        const int chunk = 2 * kk + k_hi;                     // 16-byte chunk along D
+        const uint32_t addr = kbase + (chunk >> 3) * kBox16Bytes + k_tok * 128 +
+                              (((chunk & 7) ^ (k_tok & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(addr, a0, a1, a2, a3);
+        M::run(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+    }
+
+    // mask past the span's end, scale into log2 units
+    const bool v_lo = tok0 + r8 < t_end, v_hi8 = tok0 + r8 + 8 < t_end;
+    const float x0 = v_lo ? sc[0] * scale_log2 : -INFINITY;    // (r8,   hA)
+    const float x1 = v_lo ? sc[1] * scale_log2 : -INFINITY;    // (r8,   hB)
+    const float x2 = v_hi8 ? sc[2] * scale_log2 : -INFINITY;   // (r8+8, hA)
+    const float x3 = v_hi8 ? sc[3] * scale_log2 : -INFINITY;   // (r8+8, hB)
+    float xa = fmaxf(x0, x2), xb = fmaxf(x1, x3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, o));
+    }
+    s.tA = fmaxf(s.tA, xa);
+    s.tB = fmaxf(s.tB, xb);
+    const bool raiseA = xa > s.mA + kRescaleThresholdLog2;
+    const bool raiseB = xb > s.mB + kRescaleThresholdLog2;
+    if (__any_sync(0xffffffffu, raiseA || raiseB)) {
+        const float nA = raiseA ? xa : s.mA, nB = raiseB ? xb : s.mB;
+        const float fA = ex2(s.mA - nA), fB = ex2(s.mB - nB);
+#pragma unroll
+        for (int n = 0; n < kKSteps; ++n) {
+            s.acc[n][0] *= fA;
+            s.acc[n][1] *= fB;
+            s.acc[n][2] *= fA;
+            s.acc[n][3] *= fB;
+        }
+        s.lA *= fA;
+        s.lB *= fB;
+        s.mA = nA;
+        s.mB = nB;
+    }
+    // P in the 16-bit type; P^T fragments by an in-register transpose
+    const float e0 = ex2(x0 - s.mA), e1 = ex2(x1 - s.mB);   // token r8
+    const float e2 = ex2(x2 - s.mA), e3 = ex2(x3 - s.mB);   // token r8+8
+    const uint32_t p01 = M::pack(e0, e1);
+    const uint32_t p23 = M::pack(e2, e3);
+    const uint32_t pb0 = movmatrix_trans(p01);   // (head r8, tokens 2c4..+1)
+    const uint32_t pb1 = movmatrix_trans(p23);   // (head r8, tokens 8+2c4..+1)
+    uint32_t pl0 = 0u, pl1 = 0u;
+    if (kSplitP) {
+        const float2 u = M::unpack(p01), w = M::unpack(p23);
+        pl0 = movmatrix_trans(M::pack(e0 - u.x, e1 - u.y));
+        pl1 = movmatrix_trans(M::pack(e2 - w.x, e3 - w.y));
+        s.lA += e0 + e2;
+        s.lB += e1 + e3;
+    } else {
+        const float2 u = M::unpack(p01), w = M::unpack(p23);
+        s.lA += u.x + w.x;
+        s.lB += u.y + w.y;
+    }
+
+    // ragged tail: zero V rows past the end so that 0 * V stays 0
+    if (tok0 + kTileTokens > t_end) {
+        const int valid = t_end - tok0;
+        const int rows = kTileTokens - valid;
+        for (int idx = lane; idx < (D / 64) * rows * 8; idx += 32) {
+            const int hh = idx / (rows * 8);
+            const int rem = idx - hh * rows * 8;
+            const int rr = valid + (rem >> 3);
+            *reinterpret_cast<uint4*>(vtile + hh * kBox16Bytes + rr * 128 + ((rem & 7) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    // O^T += V^T . P^T, one m16n8k16 per 16-dim slab
+#pragma unroll
+    for (int n = 0; n < kKSteps; ++n) {
+        const int chunk = 2 * n + v_hi;
+        const uint32_t addr = vbase + (chunk >> 3) * kBox16Bytes + v_tok * 128 +
+                              (((chunk & 7) ^ (v_tok & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(addr, a0, a1, a2, a3);
+        M::run(s.acc[n], a0, a1, a2, a3, pb0, pb1);
+        if (kSplitP) M::run(s.acc[n], a0, a1, a2, a3, pl0, pl1);
+    }
+}
+
+}  // namespace pa

@@ -68,6 +68,44 @@ struct DecodeParams {
     float v_scale;
 };
 
+// Work-balanced fused step (balanced.cu).
+struct BalancedParams {
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    void* out;
+    int* err;
+    float scale_log2;
+    int num_q_heads;
+    int group;
+    int max_blocks_per_seq;
+    int block_size;
+    int64_t num_blocks;
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slot_mapping;
+    void* k_cache;
+    void* v_cache;
+    int* counters;                 // [B][Hkv], 0 on entry and on exit
+    int num_kv_heads;
+    float k_scale;
+    float v_scale;
+    int num_seqs;
+    int num_warps;                 // consumer warps of the grid
+    int* plan;                     // [N, Q, prefix[B + 1]]
+    float* rec_o;                  // [R][G][D] partial outputs, R = num_warps + B * Hkv
+    float* rec_m;                  // [R][G]
+    float* rec_l;                  // [R][G]
+};
+
+// Layout of the balanced step's plan (ints): [N, Q, prefix[B + 1], pad,
+// start cursors int4[num_warps] from this offset on (16-byte aligned).
+__host__ __device__ __forceinline__ int plan_starts_offset(int B) { return ((B + 3 + 3) / 4) * 4; }
+
+cudaError_t launch_balanced(int dtype, int head_dim, bool fp8, const CUtensorMap& tmk,
+                            const CUtensorMap& tmv, const BalancedParams& p, int num_ctas,
+                            cudaStream_t stream);
+
 // Decode kernel modes.
 constexpr int kModeSingle = 0;   // one CTA per (sequence, KV head), final output
 constexpr int kModeSplit = 1;    // one CTA per partition, partial outputs

@@ -73,6 +73,14 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         for fn in ("pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_decode_split_fp8",
                    "pa_decode_step_fp8"):
             getattr(lib, fn).restype = ctypes.c_int
+        lib.pa_balanced_workspace_size.argtypes = [S]
+        lib.pa_balanced_workspace_size.restype = ctypes.c_size_t
+        lib.pa_decode_step_balanced.argtypes = [V, V, V, V, V, V, V, V, F, V, ctypes.c_size_t, V,
+                                                S, V]
+        lib.pa_decode_step_balanced_fp8.argtypes = [V, V, V, V, V, V, V, V, F, F, F, V,
+                                                    ctypes.c_size_t, V, S, V]
+        lib.pa_decode_step_balanced.restype = ctypes.c_int
+        lib.pa_decode_step_balanced_fp8.restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [V, V, I64, V, V, I64, V, I64, S, V]
         lib.pa_copy_blocks.restype = ctypes.c_int
         lib.pa_decode_step.argtypes = [V, V, V, V, V, V, V, V, F, I32, I32, V, V, V, V, V, S, V]
@@ -459,6 +467,56 @@ def decode_step(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, c
     return out
 
 
+def balanced_workspace(q: torch.Tensor, k_cache: torch.Tensor,
+                       block_tables: torch.Tensor) -> torch.Tensor:
+    """Zeroed workspace for ``decode_step_balanced`` (reusable across steps)."""
+    if k_cache.dtype == torch.uint8:
+        shp = _fp8_shape(q.shape[0], q.shape[1], k_cache, block_tables.shape[1], q.dtype)
+    else:
+        shp = make_shape(q.shape[0], q.shape[1], k_cache, block_tables.shape[1])
+    with torch.cuda.device(q.device):
+        n = int(load().pa_balanced_workspace_size(ctypes.byref(shp)))
+    if n == 0:
+        raise PaError("pa_balanced_workspace_size", PA_ERR_INVALID_ARG)
+    return torch.zeros(n, dtype=torch.uint8, device=q.device)
+
+
+def decode_step_balanced(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                         context_lens, scale: float, out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, k_scale: float = None,
+                         v_scale: float = None) -> torch.Tensor:
+    """Fused decode layer-step with the work balanced over one wave of CTAs
+    (pa_decode_step_balanced; pa_decode_step_balanced_fp8 for a uint8 E4M3
+    cache with k_scale / v_scale)."""
+    lib = load()
+    fp8 = k_cache.dtype == torch.uint8
+    if fp8:
+        shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens)
+    else:
+        shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, n, q.dtype, dev)
+    _need(slot_mapping, "slot_mapping", torch.int64, dev)
+    if k_new.shape != (q.shape[0], k_cache.shape[2], k_cache.shape[3]) or \
+            v_new.shape != k_new.shape or slot_mapping.shape != (q.shape[0],):
+        raise ValueError("k_new / v_new must be [num_seqs][num_kv_heads][head_dim], "
+                         "slot_mapping [num_seqs]")
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", q.dtype, dev)
+    if workspace is None:
+        workspace = balanced_workspace(q, k_cache, block_tables)
+    _need(workspace, "workspace", torch.uint8, dev)
+    args = [_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), _ptr(context_lens), ctypes.c_float(scale)]
+    if fp8:
+        args += [ctypes.c_float(k_scale), ctypes.c_float(v_scale)]
+    args += [_ptr(workspace), ctypes.c_size_t(workspace.numel()), _ptr(out), ctypes.byref(shp),
+             _stream_handle(dev)]
+    fn = lib.pa_decode_step_balanced_fp8 if fp8 else lib.pa_decode_step_balanced
+    _check("pa_decode_step_balanced" + ("_fp8" if fp8 else ""), fn(*args))
+    return out
+
+
 STATIC_WORKSPACE_BYTES = 32 << 20
 
 
@@ -553,8 +611,8 @@ class StepPlan:
         if self.fp8:
             if k_scale is None or v_scale is None:
                 raise ValueError("an FP8 cache needs k_scale and v_scale")
-            if mode not in ("auto", "fused"):
-                raise ValueError("StepPlan runs an FP8 cache through the fused step only")
+            if mode not in ("auto", "fused", "balanced"):
+                raise ValueError("StepPlan runs an FP8 cache through the fused steps only")
             shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens)
         else:
             shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
@@ -569,9 +627,9 @@ class StepPlan:
         _need(self.out, "out", q.dtype, dev)
         if mode == "auto":
             mode = "fused"
-        if mode not in ("single", "split", "fused"):
+        if mode not in ("single", "split", "fused", "balanced"):
             raise ValueError(f"unknown mode {mode!r}")
-        if mode == "fused" and T != q.shape[0]:
+        if mode in ("fused", "balanced") and T != q.shape[0]:
             raise ValueError("the fused step takes exactly one new token per sequence")
         self.mode = mode
         self.partition_size = int(partition_size)
@@ -585,6 +643,17 @@ class StepPlan:
         if mode == "single":
             self._decode_args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                  _ptr(context_lens), ctypes.c_float(scale), _ptr(self.out), sref)
+        elif mode == "balanced":
+            if workspace is None:
+                workspace = balanced_workspace(q, k_cache, block_tables)
+            self.workspace = workspace
+            self._keep.append(workspace)
+            scales = (ctypes.c_float(k_scale), ctypes.c_float(v_scale)) if self.fp8 else ()
+            self._step_args = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                               _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                               _ptr(context_lens), ctypes.c_float(scale), *scales,
+                               _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                               _ptr(self.out), sref)
         elif mode == "fused":
             if workspace is None:
                 workspace = step_workspace(q, k_cache.shape[2], self.num_partitions)
@@ -622,13 +691,17 @@ class StepPlan:
         return ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
 
     def reshape_and_cache(self):
-        if self.mode == "fused":
+        if self.mode in ("fused", "balanced"):
             return                          # part of the fused step
         _check("pa_reshape_and_cache",
                self._lib.pa_reshape_and_cache(*self._reshape_args, self._stream()))
 
     def decode(self):
-        if self.mode == "fused" and self.fp8:
+        if self.mode == "balanced":
+            fn = self._lib.pa_decode_step_balanced_fp8 if self.fp8 else \
+                self._lib.pa_decode_step_balanced
+            _check("pa_decode_step_balanced", fn(*self._step_args, self._stream()))
+        elif self.mode == "fused" and self.fp8:
             _check("pa_decode_step_fp8",
                    self._lib.pa_decode_step_fp8(*self._step_args, self._stream()))
         elif self.mode == "fused":

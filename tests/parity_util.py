@@ -42,7 +42,8 @@ def gpu_bits(t: torch.Tensor) -> np.ndarray:
     return pin.bits(t.cpu())
 
 
-def check_workload(w: pin.Workload, dev, modes=("single", "split", "fused"), partition_size=512,
+def check_workload(w: pin.Workload, dev, modes=("single", "split", "fused", "balanced"),
+                   partition_size=512,
                    check_partitions=True):
     """Cache write bit-exact, then decode through each mode against the oracle.
     Returns a dict of max errors."""
@@ -60,20 +61,28 @@ def check_workload(w: pin.Workload, dev, modes=("single", "split", "fused"), par
     errs = {}
     max_len = int(w.context_lens.max()) if w.num_seqs else 0
     for mode in modes:
-        if mode == "fused":
-            # one launch from the unwritten caches: cache write + attention + merge
+        if mode in ("fused", "balanced"):
+            # one step from the unwritten caches: cache write + attention + merge
             kc = w.k_cache.to(dev)
             vc = w.v_cache.to(dev)
-            S = lib.num_partitions(max_len, partition_size)
-            ws = lib.step_workspace(d["q"], w.num_kv_heads, S)
-            out = lib.decode_step(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], kc, vc,
-                                  d["block_tables"], d["context_lens"], w.scale, max_len,
-                                  partition_size=partition_size, workspace=ws)
+            if mode == "fused":
+                S = lib.num_partitions(max_len, partition_size)
+                ws = lib.step_workspace(d["q"], w.num_kv_heads, S)
+                out = lib.decode_step(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], kc, vc,
+                                      d["block_tables"], d["context_lens"], w.scale, max_len,
+                                      partition_size=partition_size, workspace=ws)
+                counters = ws[3]
+            else:
+                ws = lib.balanced_workspace(d["q"], kc, d["block_tables"])
+                out = lib.decode_step_balanced(d["q"], d["k_new"], d["v_new"], d["slot_mapping"],
+                                               kc, vc, d["block_tables"], d["context_lens"],
+                                               w.scale, workspace=ws)
+                counters = ws[:w.num_seqs * w.num_kv_heads * 4]
             torch.cuda.synchronize(dev)
-            assert np.array_equal(gpu_bits(kc), kc_ref), "fused step: k_cache differs"
-            assert np.array_equal(gpu_bits(vc), vc_ref), "fused step: v_cache differs"
-            assert int(ws[3].abs().sum()) == 0, "fused step left counters non-zero"
-            errs[mode] = assert_close(out.float().cpu().numpy(), want, f"{w.name} fused out")
+            assert np.array_equal(gpu_bits(kc), kc_ref), f"{mode} step: k_cache differs"
+            assert np.array_equal(gpu_bits(vc), vc_ref), f"{mode} step: v_cache differs"
+            assert int(counters.abs().sum()) == 0, f"{mode} step left counters non-zero"
+            errs[mode] = assert_close(out.float().cpu().numpy(), want, f"{w.name} {mode} out")
             continue
         if mode == "single":
             out = lib.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],

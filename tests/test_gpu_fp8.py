@@ -75,6 +75,13 @@ def _check_fp8(w, kc, vc, dev, partition_size=512):
     torch.cuda.synchronize(dev)
     assert np.array_equal(kd.cpu().numpy(), wk) and np.array_equal(vd.cpu().numpy(), wv)
     assert_close(out.float().cpu().numpy(), want, f"{w.name} fp8 fused step")
+    # the balanced step from the unwritten cache
+    kb, vb = kc.to(dev), vc.to(dev)
+    outb = lib.decode_step_balanced(d["q"], d["k_new"], d["v_new"], d["sm"], kb, vb, d["bt"],
+                                    d["cl"], w.scale, k_scale=K_SCALE, v_scale=V_SCALE)
+    torch.cuda.synchronize(dev)
+    assert np.array_equal(kb.cpu().numpy(), wk) and np.array_equal(vb.cpu().numpy(), wv)
+    assert_close(outb.float().cpu().numpy(), want, f"{w.name} fp8 balanced step")
     # single pass and split + merge over the written cache
     single = lib.decode_fp8(d["q"], kd, vd, d["bt"], d["cl"], w.scale, K_SCALE, V_SCALE)
     assert_close(single.float().cpu().numpy(), want, f"{w.name} fp8 single")

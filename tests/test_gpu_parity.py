@@ -53,7 +53,7 @@ def test_edge_lengths(dev, dtype, hq, hkv, d, bs):
                                        block_size=bs), seed=hq * 7 + d + bs)
     for P in sorted({bs, 2 * bs, 64 if 64 % bs == 0 else bs, 512}):
         check_workload(w, dev, modes=("split", "fused"), partition_size=P)
-    check_workload(w, dev, modes=("single",))
+    check_workload(w, dev, modes=("single", "balanced"))
 
 
 def test_single_partition_split_matches_single_pass(dev):
@@ -145,7 +145,7 @@ def test_non_default_stream(dev):
     assert_close(out.float().cpu().numpy(), want, "side stream")
 
 
-@pytest.mark.parametrize("mode", ["single", "split", "fused"])
+@pytest.mark.parametrize("mode", ["single", "split", "fused", "balanced"])
 def test_step_plan_eager_and_graph_replay(dev, mode):
     """The prepared step (and its CUDA-graph replay) equals the plain calls."""
     w = pin.build_workload(params=dict(dtype="bf16", num_seqs=9, lens=[1, 16, 33, 100, 600, 1000,
