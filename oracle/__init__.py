@@ -79,6 +79,9 @@ def _load():
             lib.oracle_paged_decode_fp8.restype = i32
             lib.oracle_paged_decode_fp8.argtypes = [P, P, P, P, P, f64, f64, f64, i32, i32, i32,
                                                     i32, i32, i32, i32, P]
+            lib.oracle_paged_prefill.restype = i32
+            lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, f64, i32, i32, i32, i32, i32,
+                                                 i32, i32, P]
             lib.oracle_copy_blocks.restype = i64
             lib.oracle_copy_blocks.argtypes = [P, P, i64, P, P, i64, P, i64, i32, i32, i32]
             lib.oracle_max_threads.restype = i32
@@ -293,6 +296,29 @@ def paged_decode_partitions(q, k_cache, v_cache, block_tables, context_lens, sca
     if rc != 0:
         raise ValueError("oracle_paged_decode_partitions: bad arguments")
     return po, pm, ps
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
+                  dtype: str) -> np.ndarray:
+    """fp64 causal attention of every new token of every sequence
+    ([total_tokens][Hq][D]); new tokens are the last C_b of each context."""
+    q = _u16(q)
+    kc, vc = _u16(k_cache), _u16(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    B = cl.shape[0]
+    total, hq, d = q.shape
+    nb, bs, hkv, d2 = kc.shape
+    assert d2 == d and qs.shape == (B + 1,) and int(qs[-1]) == total and bt.shape[0] == B
+    assert np.all(np.diff(qs) <= cl) and np.all(np.diff(qs) >= 0)
+    out = np.zeros((total, hq, d), dtype=np.float64)
+    rc = _load().oracle_paged_prefill(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl), _ptr(qs),
+                                      float(scale), B, hq, hkv, d, bs, bt.shape[1],
+                                      _DTYPES[dtype], _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_paged_prefill: bad shape")
+    return out
 
 
 def lse_merge(part_out, part_max, part_sum, context_lens, partition_size: int) -> np.ndarray:

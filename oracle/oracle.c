@@ -295,6 +295,44 @@ int oracle_paged_decode(const uint16_t* q, const uint16_t* k_cache,
 }
 
 /*
+ * Paged prefill / chunked prefill: sequence b has C_b = query_start[b+1] -
+ * query_start[b] new tokens, the last C_b of its L_b = context_lens[b] tokens
+ * (all already in the cache).  New token i sits at position
+ * p = L_b - C_b + i and attends causally to positions 0..p:
+ *   out[query_start[b] + i][h] = softmax_{j <= p}(scale * q . K_j) . V_j
+ * (ta-paperlens page, prefill vs decode and chunked prefill; techfeed summary,
+ * chunked prefill splits a long prompt across forward passes).  q and out are
+ * [total_tokens][num_q_heads][head_dim].
+ */
+int oracle_paged_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                         const int32_t* block_tables, const int32_t* context_lens,
+                         const int32_t* query_start, double scale, int num_seqs,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int max_blocks_per_seq, int dtype, double* out) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
+    int G = num_q_heads / num_kv_heads;
+    int64_t total = query_start[num_seqs];
+    int64_t rows = total * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t tok = r / num_q_heads;
+        int h = (int)(r % num_q_heads);
+        int b = 0;
+        while (query_start[b + 1] <= tok) ++b;           /* the token's sequence */
+        int64_t C = query_start[b + 1] - query_start[b];
+        int64_t p = context_lens[b] - C + (tok - query_start[b]);
+        double* qrow = (double*)malloc((size_t)head_dim * sizeof(double));
+        for (int d = 0; d < head_dim; ++d) qrow[d] = widen(q[r * head_dim + d], dtype);
+        double m, l;
+        attend_span(qrow, k_cache, v_cache, block_tables + (int64_t)b * max_blocks_per_seq, 0,
+                    p + 1, h / G, num_kv_heads, head_dim, block_size, dtype, scale,
+                    out + r * head_dim, &m, &l);
+        free(qrow);
+    }
+    return 0;
+}
+
+/*
  * Per-partition results of the context split: partition s of sequence b
  * covers tokens [s*P, min((s+1)*P, L_b)).  For each (b, h, s) with
  * s*P < L_b it writes

@@ -408,6 +408,105 @@ def fp8_codes(rng: np.random.Generator, shape, scale: float) -> torch.Tensor:
     return x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
 
 
+@dataclass
+class PrefillWorkload:
+    """A chunked-prefill batch: sequence b holds L_b tokens, the last C_b of
+    them new in this step (their slots from append_token, their K/V in
+    k_new / v_new, their queries in q)."""
+    name: str
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    context_lens: np.ndarray          # int32 [B]
+    query_start: np.ndarray           # int32 [B + 1]
+    block_tables: np.ndarray          # int32 [B][MB]
+    slot_mapping: np.ndarray          # int64 [T], T = sum C_b
+    q: torch.Tensor                   # [T][Hq][D]
+    k_new: torch.Tensor               # [T][Hkv][D]
+    v_new: torch.Tensor
+    k_cache: torch.Tensor             # [NB][bs][Hkv][D], before the write
+    v_cache: torch.Tensor
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start[-1])
+
+    def flops(self) -> int:
+        """Score and value products of the causal attention: 4*D per
+        (query row, visible key)."""
+        hq, d = self.num_q_heads, self.head_dim
+        total = 0
+        for b in range(self.num_seqs):
+            L, C = int(self.context_lens[b]), int(self.query_start[b + 1] - self.query_start[b])
+            total += sum(L - C + i + 1 for i in range(C))
+        return 4 * d * hq * total
+
+    def kv_bytes(self) -> int:
+        return int(self.context_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 4
+
+
+PREFILL_CONFIGS = {
+    # chunked prefill of Llama-3-8B-shaped layers: 4 sequences, 512-token
+    # chunks appended to contexts of 0..3584 earlier tokens
+    "prefill8b": (20270, dict(dtype="bf16", lens=[512, 1536, 2560, 4096], chunks=[512] * 4,
+                              num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16)),
+    "prefill_tiny": (20271, dict(dtype="fp16", lens=[1, 20, 64, 100], chunks=[1, 20, 17, 33],
+                                 num_q_heads=8, num_kv_heads=2, head_dim=64, block_size=16)),
+}
+
+
+def build_prefill_workload(name: Optional[str] = None, seed: Optional[int] = None,
+                           params: Optional[dict] = None, pool_slack: float = 0.10):
+    """Seeded chunked-prefill batch (same recipe as ``build_workload``: the
+    pool permutation, then q, new K, new V, K pool, V pool)."""
+    if params is None:
+        base_seed, params = PREFILL_CONFIGS[name]
+        seed = base_seed if seed is None else seed
+    else:
+        seed = 0 if seed is None else seed
+        name = name or "custom"
+    p = params
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(p["lens"], dtype=np.int64)
+    chunks = np.asarray(p["chunks"], dtype=np.int64)
+    if np.any(chunks > lens) or np.any(chunks < 0):
+        raise ValueError("a chunk is longer than its context")
+    B, bs = len(lens), p["block_size"]
+    hq, hkv, d, dt = p["num_q_heads"], p["num_kv_heads"], p["head_dim"], p["dtype"]
+    need = sum(max(1, -(-int(n) // bs)) for n in lens)
+    nb = int(p.get("num_blocks") or math.ceil(need * (1.0 + pool_slack)))
+    pool = BlockPool(nb, bs, order=rng.permutation(nb))
+    alloc = PagedKVAllocator(pool)
+    slots = []
+    for b in range(B):
+        alloc.add_sequence(b)
+        alloc.extend(b, int(lens[b] - chunks[b]))
+        slots += [alloc.append_token(b) for _ in range(int(chunks[b]))]
+    T = int(chunks.sum())
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    return PrefillWorkload(
+        name=name, dtype=dt, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+        num_blocks=nb, scale=1.0 / math.sqrt(d), context_lens=lens.astype(np.int32),
+        query_start=qs, block_tables=alloc.table_array(range(B)),
+        slot_mapping=np.asarray(slots, dtype=np.int64),
+        q=normal_tensor(rng, (T, hq, d), dt), k_new=normal_tensor(rng, (T, hkv, d), dt),
+        v_new=normal_tensor(rng, (T, hkv, d), dt),
+        k_cache=normal_tensor(rng, (nb, bs, hkv, d), dt),
+        v_cache=normal_tensor(rng, (nb, bs, hkv, d), dt))
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """Raw uint16 bit patterns of a CPU fp16/bf16 tensor (no copy)."""
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -511,3 +511,48 @@ def test_fp8_decode_matches_sdpa_on_dequantised_cache(dtype):
         o = torch.nn.functional.scaled_dot_product_attention(
             torch.from_numpy(q[b]).unsqueeze(1), K, V, scale=w.scale)[:, 0].numpy()
         np.testing.assert_allclose(got[b], o, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# paged prefill (chunked prefill): causal attention of the new tokens
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,hq,hkv,d", [("fp16", 8, 2, 64), ("bf16", 16, 4, 128)])
+def test_prefill_matches_causal_sdpa(dtype, hq, hkv, d):
+    w = pin.build_prefill_workload(params=dict(dtype=dtype, lens=[1, 17, 40, 96],
+                                               chunks=[1, 17, 9, 33], num_q_heads=hq,
+                                               num_kv_heads=hkv, head_dim=d, block_size=16),
+                                   seed=5)
+    qb, kcb, vcb = pin.bits(w.q), pin.bits(w.k_cache), pin.bits(w.v_cache)
+    got = oracle.paged_prefill(qb, kcb, vcb, w.block_tables, w.context_lens, w.query_start,
+                               w.scale, dtype)
+    kc, vc = oracle.widen(kcb, dtype), oracle.widen(vcb, dtype)
+    q = oracle.widen(qb, dtype)
+    G = hq // hkv
+    for b in range(w.num_seqs):
+        L = int(w.context_lens[b])
+        s0, s1 = int(w.query_start[b]), int(w.query_start[b + 1])
+        C = s1 - s0
+        idx = np.arange(L)
+        phys = w.block_tables[b][idx // 16]
+        K = torch.from_numpy(kc[phys, idx % 16]).permute(1, 0, 2).repeat_interleave(G, 0)
+        V = torch.from_numpy(vc[phys, idx % 16]).permute(1, 0, 2).repeat_interleave(G, 0)
+        Q = torch.from_numpy(q[s0:s1]).permute(1, 0, 2)               # [Hq][C][D]
+        pos = L - C + torch.arange(C)
+        mask = torch.arange(L)[None, :] <= pos[:, None]               # [C][L]
+        o = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask,
+                                                             scale=w.scale)
+        np.testing.assert_allclose(got[s0:s1], o.permute(1, 0, 2).numpy(), rtol=1e-12,
+                                   atol=1e-12)
+
+
+def test_prefill_of_one_token_is_decode():
+    w = pin.build_prefill_workload(params=dict(dtype="bf16", lens=[5, 64, 200],
+                                               chunks=[1, 1, 1], num_q_heads=8,
+                                               num_kv_heads=2, head_dim=64, block_size=16),
+                                   seed=8)
+    qb, kcb, vcb = pin.bits(w.q), pin.bits(w.k_cache), pin.bits(w.v_cache)
+    pre = oracle.paged_prefill(qb, kcb, vcb, w.block_tables, w.context_lens, w.query_start,
+                               w.scale, "bf16")
+    dec = oracle.paged_decode(qb, kcb, vcb, w.block_tables, w.context_lens, w.scale, "bf16")
+    assert np.array_equal(pre, dec)
