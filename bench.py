@@ -529,14 +529,108 @@ def bench_copy(args):
     return 0
 
 
+def prefill_flops(w) -> int:
+    """Algorithmic FLOPs of one chunked-prefill call: new token at position p
+    of a head attends p + 1 keys, 2 D FLOPs for its score and 2 D for its
+    share of P V each."""
+    lens = w.context_lens.astype(np.int64)
+    chunks = np.diff(w.query_start).astype(np.int64)
+    attended = 0
+    for L, C in zip(lens, chunks):
+        first = L - C + 1                       # keys seen by the first new token
+        attended += C * first + C * (C - 1) // 2
+    return int(4 * w.head_dim * w.num_q_heads * attended)
+
+
+def bench_prefill(args):
+    """Chunked-prefill attention (pa_prefill) over the paged cache: every new
+    token of every sequence attends causally through its block table."""
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pa_build.build()
+    lib.load()
+    w = pin.build_prefill_workload(args.prefill_config,
+                                   seed=pin.PREFILL_CONFIGS[args.prefill_config][0] + 1000 * rank)
+    d = {k: v.to(dev) if isinstance(v, torch.Tensor) else torch.from_numpy(v).to(dev)
+         for k, v in dict(q=w.q, kn=w.k_new, vn=w.v_new, kc=w.k_cache, vc=w.v_cache,
+                          bt=w.block_tables, cl=w.context_lens, qs=w.query_start,
+                          sm=w.slot_mapping).items()}
+    lib.reshape_and_cache(d["kn"], d["vn"], d["sm"], d["kc"], d["vc"])
+    max_q = int(np.diff(w.query_start).max())
+    out = torch.empty_like(d["q"])
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q, out)
+
+    for _ in range(args.warmup):
+        flush(1.0)
+        call()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    import torch.distributed as dist
+    sync_ranks = dist.is_available() and dist.is_initialized()
+    with ClockSampler(local_rank) as clocks:
+        time.sleep(0.2)
+        if sync_ranks:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = time.time()
+        for i in range(args.steps):
+            flush(float(i))
+            evs[i][0].record(stream)
+            call()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_end = time.time()
+        if sync_ranks:
+            dist.barrier()
+        time.sleep(0.2)
+    clk = clocks.summary(t_start, t_end)
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, dev)
+    flops = prefill_flops(w)
+    tflops = flops * world / (ms * 1e-3) / 1e12
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peak = float(json.load(f)["bf16_tflops"])
+    kv_tokens = int(w.context_lens.sum())
+    kv_bytes = kv_tokens * w.num_kv_heads * w.head_dim * 2 * 2
+    line = {"metric": "chunked-prefill attention TFLOP/s over the paged cache",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
+            "config": {"workload": f"{w.name}: {pin.PREFILL_DESCRIPTIONS[w.name]}",
+                       "new_tokens": int(w.query_start[-1]), "kv_tokens": kv_tokens,
+                       "kv_bytes": kv_bytes, "flops_per_call": flops,
+                       "l2": "flushed before every call (outside its events)"},
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill", "achieved": round(tflops / world, 2),
+                         "peak": peak, "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, "
+                                                      "burst; mma.sync m16n8k16 path)",
+                         "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4),
+                         "traffic": None},
+            "clocks": clk, "gpu_launches": args.steps,
+            "device_errors": lib.read_device_errors(dev)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["step", "copy"], default="step",
-                    help="what to time: the decode layer-step, or whole-block copies")
+    ap.add_argument("--op", choices=["step", "copy", "prefill"], default="step",
+                    help="what to time: the decode layer-step, whole-block copies, or "
+                         "chunked-prefill attention")
+    ap.add_argument("--prefill-config", default="prefill8b", choices=sorted(pin.PREFILL_CONFIGS))
     ap.add_argument("--config", default="llama8b", choices=sorted(pin.CONFIGS))
     ap.add_argument("--mode", default="auto", choices=["auto", "single", "split", "fused",
                                                        "balanced"])
@@ -553,6 +647,8 @@ def main(argv=None):
         return bench_reference(args)
     if args.op == "copy":
         return bench_copy(args)
+    if args.op == "prefill":
+        return bench_prefill(args)
     return bench_ours(args)
 
 

@@ -228,6 +228,26 @@ int pa_decode_step_balanced_fp8(const void* q, const void* k, const void* v,
                                 void* stream);
 
 /*
+ * pa_prefill: paged prefill / chunked-prefill attention.  Sequence b holds
+ * L_b = context_lens[b] tokens in the cache, the last C_b = query_start[b+1]
+ * - query_start[b] of which are new in this step (written beforehand with
+ * pa_reshape_and_cache).  New token i of b sits at position p = L_b - C_b + i
+ * and attends causally:
+ *   out[query_start[b] + i][h][:] = sum_{j <= p} softmax_j(scale q.K_j) V_j
+ * (ta-paperlens page, prefill vs decode and chunked prefill; techfeed
+ * summary, chunked prefill of long prompts).  A one-token chunk is a decode.
+ * q, out: [total_tokens][num_q_heads][head_dim] with total_tokens =
+ * query_start[num_seqs]; query_start int32 [num_seqs + 1], non-decreasing,
+ * from 0; max_query_len >= every C_b (it sizes the grid: query tokens past
+ * 16 * ceil(max_query_len / 16) are not computed).  C_b > L_b is clamped to
+ * L_b and flagged (PA_DEVERR_BAD_CONTEXT).  All pointers device.
+ */
+int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, const int32_t* context_lens,
+               const int32_t* query_start, float scale, int32_t max_query_len, void* out,
+               const pa_shape* shp, void* stream);
+
+/*
  * pa_copy_blocks: copy whole physical blocks between two block pools.  For
  * each pair p < num_pairs of block_mapping (int64 [num_pairs][2], device):
  *   src = block_mapping[2p], dst = block_mapping[2p+1],

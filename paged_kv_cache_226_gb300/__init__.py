@@ -7,7 +7,7 @@ block allocator and seeded workload builder.
 from . import inputs  # noqa: F401
 from .lib import (  # noqa: F401
     DEFAULT_PARTITION, PaError, copy_blocks, decode, decode_split, decode_step,
-    decode_step_balanced, load,
+    decode_step_balanced, load, prefill,
     num_partitions,
     paged_attention,
     StepPlan, read_device_errors, reduce, reshape_and_cache, split_workspace,

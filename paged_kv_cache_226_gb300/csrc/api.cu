@@ -552,6 +552,43 @@ int pa_decode_step_fp8(const void* q, const void* k, const void* v, const int64_
                        counters, out, shp, stream, CacheKind{true, k_scale, v_scale});
 }
 
+int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, const int32_t* context_lens,
+               const int32_t* query_start, float scale, int32_t max_query_len, void* out,
+               const pa_shape* shp, void* stream) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if (max_query_len < 0) return PA_ERR_INVALID_ARG;
+    if (shp->num_seqs == 0 || max_query_len == 0) return PA_OK;
+    if (!query_start || (reinterpret_cast<uintptr_t>(query_start) & 3u) || !out || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    const int64_t qtiles = (max_query_len + 15) / 16;
+    if (qtiles > 0x7fffffffll) return PA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp, false)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp, false)) != PA_OK) return st;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::PrefillParams p{};
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start = query_start;
+    p.err = err;
+    p.scale_log2 = scale * pa::kLog2e;
+    p.num_q_heads = shp->num_q_heads;
+    p.group = shp->num_q_heads / shp->num_kv_heads;
+    p.max_blocks_per_seq = shp->max_blocks_per_seq;
+    p.block_size = shp->block_size;
+    p.num_blocks = shp->num_blocks;
+    dim3 grid((unsigned)qtiles, shp->num_kv_heads, shp->num_seqs);
+    e = pa::launch_prefill(shp->dtype, shp->head_dim, tmk, tmv, p, grid,
+                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 int pa_copy_blocks(const void* k_src, const void* v_src, int64_t src_num_blocks, void* k_dst,
                    void* v_dst, int64_t dst_num_blocks, const int64_t* block_mapping,
                    int64_t num_pairs, const pa_shape* shp, void* stream) {

@@ -106,6 +106,26 @@ cudaError_t launch_balanced(int dtype, int head_dim, bool fp8, const CUtensorMap
                             const CUtensorMap& tmv, const BalancedParams& p, int num_ctas,
                             cudaStream_t stream);
 
+// Paged prefill (prefill.cu).
+struct PrefillParams {
+    const void* q;                 // [T][Hq][D]
+    void* out;                     // [T][Hq][D]
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* query_start;    // [B + 1]
+    int* err;
+    float scale_log2;
+    int num_q_heads;
+    int group;
+    int max_blocks_per_seq;
+    int block_size;
+    int64_t num_blocks;
+};
+
+cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap& tmk,
+                           const CUtensorMap& tmv, const PrefillParams& p, dim3 grid,
+                           cudaStream_t stream);
+
 // Decode kernel modes.
 constexpr int kModeSingle = 0;   // one CTA per (sequence, KV head), final output
 constexpr int kModeSplit = 1;    // one CTA per partition, partial outputs

@@ -467,6 +467,15 @@ PREFILL_CONFIGS = {
 }
 
 
+PREFILL_DESCRIPTIONS = {
+    "prefill8b": "chunked prefill, Llama-3-8B-shaped layer: 4 sequences, 512 new tokens each "
+                 "on contexts of 512/1536/2560/4096, 32 q / 8 KV heads, head_dim 128, bf16, "
+                 "block 16",
+    "prefill_tiny": "small chunked prefill: 4 sequences, chunks 1/20/17/33 on contexts "
+                    "1/20/64/100, 8 q / 2 KV heads, head_dim 64, fp16, block 16",
+}
+
+
 def build_prefill_workload(name: Optional[str] = None, seed: Optional[int] = None,
                            params: Optional[dict] = None, pool_slack: float = 0.10):
     """Seeded chunked-prefill batch (same recipe as ``build_workload``: the

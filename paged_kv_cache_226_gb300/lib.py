@@ -81,6 +81,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                     ctypes.c_size_t, V, S, V]
         lib.pa_decode_step_balanced.restype = ctypes.c_int
         lib.pa_decode_step_balanced_fp8.restype = ctypes.c_int
+        lib.pa_prefill.argtypes = [V, V, V, V, V, V, F, I32, V, S, V]
+        lib.pa_prefill.restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [V, V, I64, V, V, I64, V, I64, S, V]
         lib.pa_copy_blocks.restype = ctypes.c_int
         lib.pa_decode_step.argtypes = [V, V, V, V, V, V, V, V, F, I32, I32, V, V, V, V, V, S, V]
@@ -514,6 +516,31 @@ def decode_step_balanced(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_
              _stream_handle(dev)]
     fn = lib.pa_decode_step_balanced_fp8 if fp8 else lib.pa_decode_step_balanced
     _check("pa_decode_step_balanced" + ("_fp8" if fp8 else ""), fn(*args))
+    return out
+
+
+def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
+            max_query_len: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Chunked-prefill attention (pa_prefill): the last C_b tokens of each
+    sequence attend causally over its cache; q, out [total_tokens][Hq][D]."""
+    lib = load()
+    dev = k_cache.device
+    _need(q, "q", k_cache.dtype, dev)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, k_cache.dtype, dev)
+    _need(block_tables, "block_tables", torch.int32, dev)
+    _need(context_lens, "context_lens", torch.int32, dev)
+    _need(query_start, "query_start", torch.int32, dev)
+    B = context_lens.shape[0]
+    if query_start.shape != (B + 1,) or block_tables.shape[0] != B or q.dim() != 3:
+        raise ValueError("query_start must be [num_seqs + 1], q [total_tokens][Hq][D]")
+    out = torch.empty_like(q) if out is None else out
+    _need(out, "out", q.dtype, dev)
+    shp = make_shape(B, q.shape[1], k_cache, block_tables.shape[1])
+    _check("pa_prefill", lib.pa_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                        _ptr(context_lens), _ptr(query_start), float(scale),
+                                        int(max_query_len), _ptr(out), ctypes.byref(shp),
+                                        _stream_handle(dev)))
     return out
 
 
