@@ -399,8 +399,9 @@ MUTATIONS = {
                      "int64_t o = (i + 1) % block_size;\n    return"),
     "no_normalise": ("for (int d = 0; d < head_dim; ++d) o[d] /= l;\n    }\n    free(s);",
                      "for (int d = 0; d < head_dim; ++d) o[d] /= 1.0;\n    }\n    free(s);"),
-    "table_stride": ("block_tables + (int64_t)b * max_blocks_per_seq, 0,",
-                     "block_tables + (int64_t)b, 0,"),
+    "table_stride": ("block_tables + (int64_t)b * max_blocks_per_seq, 0,\n"
+                     "                    context_lens[b]",
+                     "block_tables + (int64_t)b, 0,\n                    context_lens[b]"),
     "k_for_v": ("const uint16_t* vr = paged_row(v_cache, table_row",
                 "const uint16_t* vr = paged_row(k_cache, table_row"),
     "exp_sign": ("double w = exp(s[i] - m);\n        l += w;\n        const uint16_t* vr = paged_row",
@@ -415,6 +416,37 @@ def _pins_pass() -> bool:
     except AssertionError:
         return False
     return True
+
+
+# mistakes in the chunked-prefill oracle, caught by the prefill pins below
+PREFILL_MUTATIONS = {
+    "prefill_origin": ("int64_t p = context_lens[b] - C + (tok - query_start[b]);",
+                       "int64_t p = tok - query_start[b];"),
+    "prefill_not_causal": ("p + 1, h / G, num_kv_heads", "context_lens[b], h / G, num_kv_heads"),
+    "prefill_gqa": ("p + 1, h / G, num_kv_heads", "p + 1, h % num_kv_heads, num_kv_heads"),
+    "prefill_includes_next": ("p + 1, h / G, num_kv_heads",
+                              "(p + 2 < context_lens[b] ? p + 2 : p + 1), h / G, num_kv_heads"),
+}
+
+
+def _prefill_pins_pass() -> bool:
+    try:
+        test_prefill_matches_causal_sdpa("bf16", 16, 4, 128)
+    except AssertionError:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL_MUTATIONS))
+def test_prefill_pins_fail_on_planted_mistake(name):
+    old, new = PREFILL_MUTATIONS[name]
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    with tempfile.TemporaryDirectory() as tmp:
+        path = oracle.compile_variant(src.replace(old, new), os.path.join(tmp, "lib_mut.so"))
+        with oracle.use_library(path):
+            assert not _prefill_pins_pass(), f"prefill pins did not catch {name}"
+    assert _prefill_pins_pass()
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
