@@ -40,7 +40,17 @@ METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; µs per layer-
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 FP8_K_SCALE, FP8_V_SCALE = 1.0 / 64, 1.0 / 48
-DECODE_KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_226_gb300", "csrc", "decode_kernel.cuh")
+_CSRC = os.path.join(ROOT, "paged_kv_cache_226_gb300", "csrc")
+_TILE_SOURCES = ["decode_tile.cuh", "pa_device.cuh", "pa_internal.h"]
+# the sources each timed kernel is compiled from: a committed DRAM-traffic
+# figure counts only while these are unchanged
+KERNEL_SOURCES = {
+    "paged_decode": ["decode_kernel.cuh"] + _TILE_SOURCES,
+    "paged_decode_split": ["decode_kernel.cuh"] + _TILE_SOURCES,
+    "paged_decode_step": ["decode_kernel.cuh"] + _TILE_SOURCES,
+    "balanced_step": ["balanced.cu"] + _TILE_SOURCES,
+    "paged_prefill": ["prefill.cu"] + _TILE_SOURCES,
+}
 
 
 def dist_env():
@@ -77,20 +87,24 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash(path=DECODE_KERNEL_SRC) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(_CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(config: str, kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    """DRAM bytes per launch from a committed ncu summary
+    (profiles/<kernel>_<config>.json), if it was taken on the kernel's current
+    sources; else None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         p = json.load(f)
-    if p.get("source_sha256_16") != source_hash():
+    if p.get("source_sha256_16") != source_hash(kernel):
         return None
     return p.get("dram_bytes_per_launch")
 
@@ -108,7 +122,8 @@ def step_bytes(w: pin.Workload, mode: str, partition: int, cache_elem_bytes: int
     split_w = parts * hq * (d + 2) * 4                  # tmp_out + max_logits + exp_sums
     kernels = {"reshape_and_cache": new_tok + write_tok + w.num_tokens * 8}
     if mode in ("fused", "balanced"):
-        kernels = {"paged_decode_step": kv + q + out + new_tok + write_tok + w.num_tokens * 8}
+        name = "paged_decode_step" if mode == "fused" else "balanced_step"
+        kernels = {name: kv + q + out + new_tok + write_tok + w.num_tokens * 8}
     elif mode == "split":
         kernels["paged_decode_split"] = kv + q + split_w
         kernels["lse_reduce"] = split_w + out
@@ -425,7 +440,7 @@ def bench_ours(args):
 
     hbm, peak_src = peaks()
     dom = {"split": "paged_decode_split", "single": "paged_decode",
-           "fused": "paged_decode_step", "balanced": "paged_decode_step"}[mode]
+           "fused": "paged_decode_step", "balanced": "balanced_step"}[mode]
     dom_ms = sum(k2_ms) / len(k2_ms)
     dom_bytes = nb["kernels"][dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -460,7 +475,8 @@ def bench_ours(args):
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "algorithmic_bytes_per_launch": dom_bytes,
-                     "traffic": profiled_traffic(args.config, dom)},
+                     "traffic": profiled_traffic(
+                         args.config + ("_fp8" if args.kv_dtype == "fp8" else ""), dom)},
         "clocks": clk.summary(t_epoch0, t_epoch1),
         "gpu_launches": {"split": 3, "single": 2, "fused": 1, "balanced": 2}[mode] * args.steps,
         "device_errors": errs,
