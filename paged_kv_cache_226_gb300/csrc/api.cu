@@ -338,7 +338,8 @@ cudaError_t balanced_grid(int* num_ctas, bool fp8) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    *num_ctas = sms * (fp8 ? pa::kMinCtasPerSmFp8 : pa::kMinCtasPerSm);
+    (void)fp8;
+    *num_ctas = sms * pa::kStreamCtasPerSm;
     return cudaSuccess;
 }
 
@@ -393,7 +394,7 @@ int decode_step_balanced(const void* q, const void* k, const void* v, const int6
     cudaError_t e = balanced_grid(&num_ctas, ck.fp8);
     if (e == cudaSuccess) e = balanced_grid(&max_ctas, false);
     if (e != cudaSuccess) return cuda_fail(e);
-    BalancedWorkspace w = balanced_layout(shp, max_ctas * pa::kConsumerWarps, workspace);
+    BalancedWorkspace w = balanced_layout(shp, max_ctas * pa::kStreamWarps, workspace);
     if (w.bytes > workspace_bytes) return PA_ERR_WORKSPACE;
     CUtensorMap tmk, tmv;
     if ((st = encode_cache_map(&tmk, k_cache, shp, ck.fp8)) != PA_OK) return st;
@@ -423,7 +424,7 @@ int decode_step_balanced(const void* q, const void* k, const void* v, const int6
     p.k_scale = ck.k_scale;
     p.v_scale = ck.v_scale;
     p.num_seqs = shp->num_seqs;
-    p.num_warps = num_ctas * pa::kConsumerWarps;
+    p.num_warps = num_ctas * pa::kStreamWarps;
     p.plan = w.plan;
     p.rec_o = w.rec_o;
     p.rec_m = w.rec_m;
@@ -441,7 +442,7 @@ size_t pa_balanced_workspace_size(const pa_shape* shp) {
     if (check_shape(shp, true) != PA_OK) return 0;
     int max_ctas = 0;
     if (balanced_grid(&max_ctas, false) != cudaSuccess) return 0;
-    return balanced_layout(shp, max_ctas * pa::kConsumerWarps, nullptr).bytes;
+    return balanced_layout(shp, max_ctas * pa::kStreamWarps, nullptr).bytes;
 }
 
 int pa_decode_step_balanced(const void* q, const void* k, const void* v,

@@ -1,15 +1,20 @@
 // Work-balanced fused decode layer-step.
 //
 // The partitioned kernels give every (sequence, KV head, partition) its own
-// CTA; for batches of many short contexts that means several waves of short
-// CTAs, each paying a start-up and drain, and a last wave that leaves SMs
-// idle.  Here the work is balanced instead: the tiles of all (sequence,
-// KV head) segments, in order, form one sequence of N 16-token tiles, and
-// consumer warp w of a single wave of CTAs streams tiles [w*Q, (w+1)*Q) with
-// Q = ceil(N / warps).  A warp crosses segment boundaries without draining
-// its pipeline; each segment piece it covers yields a partial result, and the
-// last warp to finish a segment merges its pieces (log-sum-exp) into the
-// output.  A one-CTA plan kernel first scans the per-sequence tile counts.
+// CTA; for batches of many short contexts that means more than one wave of
+// CTAs, and the CTAs that start last stream their partition alone at the end
+// of the launch, each limited by the few tiles it can keep in flight.  Here
+// the work is balanced instead: the tiles of all (sequence, KV head)
+// segments, in order, form one sequence of N 16-token tiles, and warp w of a
+// single wave of CTAs streams tiles [w*Q, (w+1)*Q) with Q = ceil(N / warps),
+// so every warp runs from the start of the launch to its end.  Each warp
+// issues the TMA loads of its own range into a private ring (no producer
+// warp, no cross-warp coupling: a warp that stops to merge holds up only its
+// own stream, whose next tiles are already in flight).  A warp crosses
+// segment boundaries without draining its ring; each segment piece it covers
+// yields a partial result, and the last warp to finish a segment merges the
+// pieces (log-sum-exp) into the output.  A one-CTA plan kernel first scans
+// the per-sequence tile counts.
 //
 // The cache write of the new token and its use by attention follow the
 // fused step (pa_decode_step).
@@ -137,17 +142,17 @@ struct TileCursor {
 };
 
 template <int D, bool kFp8>
-struct BalancedLayout {
-    static constexpr int kRing = kFp8 ? kStagesFp8 : kStages;
-    static constexpr int kPerWarp = kRing / kConsumerWarps;       // stages per consumer warp
-    static constexpr int kBoxBytes = kBox16Bytes;
+struct StreamLayout {
     static constexpr int kHalves = kFp8 ? 1 : D / kBoxElems;
-    static constexpr int kTileBytes = kHalves * kBoxBytes;
+    static constexpr int kTileBytes = kHalves * kBox16Bytes;       // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kPipeBytes = kRing * kStageBytes;
-    static constexpr int kTile16Bytes = (D / kBoxElems) * kBoxBytes;
-    static constexpr int kConvBytes = kFp8 ? kConsumerWarps * 2 * kTile16Bytes : 0;
-    static constexpr int kDynamicSmem = kPipeBytes + kConvBytes + 1024;
+    static constexpr int kTile16Bytes = (D / kBoxElems) * kBox16Bytes;
+    static constexpr int kConvBytes = kFp8 ? 2 * kTile16Bytes : 0;  // FP8: 16-bit K, V copy
+    static constexpr int kRing = (kStreamRingBytes - kConvBytes) / kStageBytes;  // stages
+    static constexpr int kWarpBytes = kRing * kStageBytes + kConvBytes;
+    static constexpr int kDynamicSmem = kStreamWarps * kWarpBytes + 1024;
+    static_assert(kRing >= 2, "a warp needs at least two stages");
+    static_assert(kWarpBytes % 1024 == 0, "warp rings must keep the 128-byte swizzle alignment");
 };
 
 // Writes the fused step's new token (chunk c of K or V, head g) into the
@@ -180,250 +185,263 @@ __device__ __forceinline__ uint4 balanced_new_token(const BalancedParams& p, int
 }
 
 // Log-sum-exp merge of the np pieces (records wfirst + j + z) of segment z by
-// one warp: lanes take pieces for the maximum and the weights, then own D/32
-// output dims each and sum the pieces, four records in flight.
+// one warp.  Lanes take pieces for the per-head maxima and weights; for the
+// weighted sum each lane owns D/32 dims of every head and keeps two pieces'
+// worth of loads (all heads) in flight.
+template <int V>
+__device__ __forceinline__ void load_vec(float (&x)[V], const float* src) {
+    if constexpr (V == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+        x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+    } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+        x[0] = v.x, x[1] = v.y;
+    }
+}
+
 template <typename T, int D>
 __device__ __forceinline__ void merge_pieces(const BalancedParams& p, int z, long long wfirst,
                                              int np, size_t qh0, int G, int lane) {
     constexpr int V = D / 32;
-    for (int h = 0; h < G; ++h) {
-        float mx = -INFINITY;
-        for (int j = lane; j < np; j += 32)
-            mx = fmaxf(mx, __ldcg(p.rec_m + (size_t)(wfirst + j + z) * G + h));
+    float mx[kMaxGroup], den[kMaxGroup], acc[kMaxGroup][V];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float acc[V];
+    for (int h = 0; h < kMaxGroup; ++h) {
+        mx[h] = -INFINITY;
+        den[h] = 0.f;
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = 0.f;
-        float den = 0.f;
-        for (int j0 = 0; j0 < np; j0 += 32) {
-            const int j = j0 + lane;
-            float wj = 0.f;
-            if (j < np) {
-                const size_t r = (size_t)(wfirst + j + z);
-                wj = __ldcg(p.rec_l + r * G + h) * ex2(__ldcg(p.rec_m + r * G + h) - mx);
+        for (int e = 0; e < V; ++e) acc[h][e] = 0.f;
+    }
+    for (int j = lane; j < np; j += 32) {
+        const size_t r = (size_t)(wfirst + j + z) * G;
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h)
+            if (h < G) mx[h] = fmaxf(mx[h], __ldcg(p.rec_m + r + h));
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxGroup; ++h) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
+    }
+    for (int j0 = 0; j0 < np; j0 += 32) {
+        const int j = j0 + lane;
+        float w[kMaxGroup];
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) w[h] = 0.f;
+        if (j < np) {
+            const size_t r = (size_t)(wfirst + j + z) * G;
+#pragma unroll
+            for (int h = 0; h < kMaxGroup; ++h)
+                if (h < G) w[h] = __ldcg(p.rec_l + r + h) * ex2(__ldcg(p.rec_m + r + h) - mx[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < kMaxGroup; ++h) den[h] += w[h];
+        const int n = min(32, np - j0);
+        for (int i = 0; i < n; i += 2) {
+            float x[2][kMaxGroup][V];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const size_t r = (size_t)(wfirst + j0 + min(i + u, n - 1) + z) * G;
+                const float* src = p.rec_o + r * D + lane * V;
+#pragma unroll
+                for (int h = 0; h < kMaxGroup; ++h)
+                    if (h < G) load_vec<V>(x[u][h], src + h * D);
             }
-            den += wj;
-            const int n = min(32, np - j0);
-            for (int i = 0; i < n; i += 4) {
-                float x[4][V], wt[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    wt[u] = __shfl_sync(0xffffffffu, wj, (i + u) & 31);
-                    const size_t r = (size_t)(wfirst + j0 + min(i + u, n - 1) + z);
-                    const float* src = p.rec_o + (r * G + h) * D + lane * V;
+            for (int u = 0; u < 2; ++u) {
+                if (i + u < n) {
 #pragma unroll
-                    for (int e = 0; e < V; ++e) x[u][e] = __ldcg(src + e);
-                }
+                    for (int h = 0; h < kMaxGroup; ++h) {
+                        if (h < G) {
+                            const float wt = __shfl_sync(0xffffffffu, w[h], i + u);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (i + u < n) {
-#pragma unroll
-                        for (int e = 0; e < V; ++e) acc[e] += wt[u] * x[u][e];
+                            for (int e = 0; e < V; ++e) acc[h][e] += wt * x[u][h][e];
+                        }
                     }
                 }
             }
         }
+    }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        T* out = reinterpret_cast<T*>(p.out) + (qh0 + h) * D + lane * V;
+    for (int h = 0; h < kMaxGroup; ++h) {
+        if (h < G) {
 #pragma unroll
-        for (int e = 0; e < V; ++e) out[e] = from_float<T>(acc[e] / den);
+            for (int o = 16; o > 0; o >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], o);
+            T* out = reinterpret_cast<T*>(p.out) + (qh0 + h) * D + lane * V;
+#pragma unroll
+            for (int e = 0; e < V; ++e) out[e] = from_float<T>(acc[h][e] / den[h]);
+        }
     }
 }
 
 template <typename T, int D, bool kFp8>
-__global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMinCtasPerSm)
+__global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
     balanced_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v,
                          const __grid_constant__ BalancedParams p) {
-    using Lay = BalancedLayout<D, kFp8>;
-    using M = Mma<T>;
+    using Lay = StreamLayout<D, kFp8>;
+    constexpr int R = Lay::kRing;
     static_assert(!kFp8 || D == 128, "the FP8 cache is built for head_dim 128");
-    __shared__ __align__(8) uint64_t full_bar[Lay::kRing];
-    __shared__ __align__(8) uint64_t empty_bar[Lay::kRing];
+    __shared__ __align__(8) uint64_t full_bar[kStreamWarps][R];
+    __shared__ int stage_blk[kStreamWarps][R];          // physical block of each staged tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+    uint8_t* ring = smem + warp * Lay::kWarpBytes;
+    uint8_t* conv = ring + R * Lay::kStageBytes;
+    uint64_t* full = full_bar[warp];
+    int* sblk = stage_blk[warp];
 
-    grid_dependency_wait();                  // the plan and the inputs are ready
-    allow_dependent_launch();
-    const int* prefix = p.plan + 2;
-    const long long N = p.plan[0];
-    const int Q = p.plan[1];
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < Lay::kRing; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
-        }
+    // the warp's own barriers and the tensor maps, before the inputs are ready
+    if (lane == 0) {
+        for (int s = 0; s < R; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
-    }
-    __syncthreads();
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------------
-        // producer: the W consumer streams' tiles, round robin, 32 at a time
-        // ------------------------------------------------------------------
-        if (lane == 0) {
+        if (warp == 0) {
             prefetch_tensor_map(&tmap_k);
             prefetch_tensor_map(&tmap_v);
         }
-        const int tiles_per_block = p.block_size / kTileTokens;
-        long long first[kConsumerWarps];
-        int count[kConsumerWarps];
-        TileCursor cur[kConsumerWarps];
-        int maxcount = 0;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const long long ws = (long long)blockIdx.x * kConsumerWarps + w;
-            first[w] = ws * Q;
-            count[w] = (int)max(0LL, min((long long)Q, N - first[w]));
-            if (count[w] > 0) cur[w].load(p.plan, B, ws);
-            maxcount = max(maxcount, count[w]);
-        }
-        // per stream: descriptors of the next 32 tiles, one per lane
-        int blk[kConsumerWarps], gg[kConsumerWarps], sub[kConsumerWarps];
-        bool ok = true;
-        for (int k0 = 0; k0 < maxcount && ok; k0 += 32) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                blk[w] = 0, gg[w] = 0, sub[w] = 0;
-                if (k0 < count[w]) {
-                    TileCursor c = cur[w];
-                    c.advance(lane, prefix, B, Hkv);
-                    if (k0 + lane < count[w]) {
-                        blk[w] = __ldg(p.block_tables + (size_t)c.b * p.max_blocks_per_seq +
-                                       c.t / tiles_per_block);
-                        if (blk[w] < 0 || blk[w] >= p.num_blocks)
-                            flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
-                        gg[w] = c.g;
-                        sub[w] = (c.t % tiles_per_block) * kTileTokens;
-                    }
-                    // the stream's cursor for the next batch: lane 31's position + 1
-                    c.advance(1, prefix, B, Hkv);
-                    cur[w].b = __shfl_sync(0xffffffffu, c.b, 31);
-                    cur[w].g = __shfl_sync(0xffffffffu, c.g, 31);
-                    cur[w].t = __shfl_sync(0xffffffffu, c.t, 31);
-                    cur[w].T = __shfl_sync(0xffffffffu, c.T, 31);
-                }
-            }
-            for (int j = 0; j < 32 && ok; ++j) {
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const int k = k0 + j;
-                    const int pb = __shfl_sync(0xffffffffu, blk[w], j);
-                    const int pg = __shfl_sync(0xffffffffu, gg[w], j);
-                    const int ps = __shfl_sync(0xffffffffu, sub[w], j);
-                    if (k >= count[w]) continue;
-                    if (lane == 0) {
-                        const int st = w + kConsumerWarps * (k % Lay::kPerWarp);
-                        const int lap = k / Lay::kPerWarp;
-                        if (lap > 0 && !mbar_wait(&empty_bar[st], (lap - 1) & 1)) {
-                            flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
-                            ok = false;
-                        } else {
-                            mbar_arrive_expect_tx(&full_bar[st], Lay::kStageBytes);
-                            uint8_t* kdst = smem + st * Lay::kStageBytes;
-                            uint8_t* vdst = kdst + Lay::kTileBytes;
-#pragma unroll
-                            for (int hh = 0; hh < Lay::kHalves; ++hh) {
-                                tma_load_4d(kdst + hh * Lay::kBoxBytes, &tmap_k, &full_bar[st],
-                                            hh * kBoxElems, pg, ps, pb);
-                                tma_load_4d(vdst + hh * Lay::kBoxBytes, &tmap_v, &full_bar[st],
-                                            hh * kBoxElems, pg, ps, pb);
-                            }
-                        }
-                    }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                }
-            }
-        }
-        return;
     }
+    __syncwarp();
+    grid_dependency_wait();                  // the plan and the inputs are ready
+    allow_dependent_launch();
 
-    // ----------------------------------------------------------------------
-    // consumer warp: its tile range, piece by piece
-    // ----------------------------------------------------------------------
-    const long long ws = (long long)blockIdx.x * kConsumerWarps + warp;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+    const int* prefix = p.plan + 2;
+    const long long N = p.plan[0];
+    const int Q = p.plan[1];
+    const long long ws = (long long)blockIdx.x * kStreamWarps + warp;
     const long long x0 = ws * Q;
     const int count = (int)max(0LL, min((long long)Q, N - x0));
     if (count == 0) return;
     const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    const int tiles_per_block = p.block_size / kTileTokens;
     const int r8 = lane >> 2, c4 = lane & 3;
     const int hA = 2 * c4, hB = 2 * c4 + 1;
-    uint8_t* conv = smem + Lay::kPipeBytes + warp * 2 * Lay::kTile16Bytes;
 
-    TileCursor cur;
+    TileCursor cur;                          // the tile being attended
     cur.load(p.plan, B, ws);
+
+    // ------------------------------------------------------------------
+    // load side: descriptors (block, KV head, token offset) of 32 tiles at a
+    // time, one per lane: set A holds the batch being issued, set B the next
+    // one, whose table reads have 32 issues' time to land.
+    // ------------------------------------------------------------------
+    TileCursor bc = cur;                     // first tile of the next batch to describe
+    int a_blk = 0, a_g = 0, a_sub = 0, b_blk = 0, b_g = 0, b_sub = 0;
+    auto describe = [&](int i0, int& blk, int& gg, int& sub) {
+        blk = 0, gg = 0, sub = 0;
+        if (i0 >= count) return;
+        TileCursor c = bc;
+        c.advance(lane, prefix, B, Hkv);
+        if (i0 + lane < count) {
+            blk = __ldg(p.block_tables + (size_t)c.b * p.max_blocks_per_seq + c.t / tiles_per_block);
+            gg = c.g;
+            sub = (c.t % tiles_per_block) * kTileTokens;
+        }
+        c.advance(1, prefix, B, Hkv);
+        bc.b = __shfl_sync(0xffffffffu, c.b, 31);
+        bc.g = __shfl_sync(0xffffffffu, c.g, 31);
+        bc.t = __shfl_sync(0xffffffffu, c.t, 31);
+        bc.T = __shfl_sync(0xffffffffu, c.T, 31);
+    };
+    describe(0, a_blk, a_g, a_sub);
+    describe(32, b_blk, b_g, b_sub);
+    // Tile j of the range into stage j % R (whole warp; lane 0 issues).
+    auto issue = [&](int j) {
+        if (j > 0 && (j & 31) == 0) {
+            a_blk = b_blk, a_g = b_g, a_sub = b_sub;
+            describe(j + 32, b_blk, b_g, b_sub);
+        }
+        const int blk = __shfl_sync(0xffffffffu, a_blk, j & 31);
+        const int gg = __shfl_sync(0xffffffffu, a_g, j & 31);
+        const int sub = __shfl_sync(0xffffffffu, a_sub, j & 31);
+        if (lane == 0) {
+            if (blk < 0 || blk >= p.num_blocks) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+            const int st = j % R;
+            sblk[st] = blk;
+            uint8_t* kdst = ring + st * Lay::kStageBytes;
+            uint8_t* vdst = kdst + Lay::kTileBytes;
+            mbar_arrive_expect_tx(&full[st], Lay::kStageBytes);
+#pragma unroll
+            for (int hh = 0; hh < Lay::kHalves; ++hh) {
+                tma_load_4d(kdst + hh * kBox16Bytes, &tmap_k, &full[st], hh * kBoxElems, gg, sub,
+                            blk);
+                tma_load_4d(vdst + hh * kBox16Bytes, &tmap_v, &full[st], hh * kBoxElems, gg, sub,
+                            blk);
+            }
+        }
+    };
+    for (int j = 0; j < R && j < count; ++j) issue(j);
+
+    // ------------------------------------------------------------------
+    // attention over the range, piece by piece
+    // ------------------------------------------------------------------
     const T* qbase = reinterpret_cast<const T*>(p.q);
     uint32_t qb[D / 16][2], qn[D / 16][2];
     TileState<D> ts;
-    // the first piece's query rows and length; later pieces' are prefetched
-    // during the last tile of the piece before
+    // the first piece's query rows, length and new-token slot; later pieces'
+    // are prefetched during the last tile of the piece before
     load_q_fragments<T, D>(qn, qbase + ((size_t)cur.b * p.num_q_heads + (size_t)cur.g * G) * D, G,
                            lane);
     int L_next = p.context_lens[cur.b];
+    int64_t slot_next = p.slot_mapping[cur.b];
     int L = 0;
+    int64_t slot = -1;
     for (int k = 0; k < count; ++k) {
         const int b = cur.b, g = cur.g, t = cur.t;
         if (k == 0 || t == 0) {                          // a piece begins
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) qb[kk][0] = qn[kk][0], qb[kk][1] = qn[kk][1];
             L = L_next < 0 ? 0 : (L_next > max_ctx ? max_ctx : L_next);
+            slot = slot_next;
             ts.reset();
         }
         const bool piece_end = (k == count - 1) || (t == cur.T - 1);
         if (piece_end && k + 1 < count) {
-            // prefetch the next piece (the next segment) while this tile runs
             TileCursor nx = cur;
             nx.advance(1, prefix, B, Hkv);
             load_q_fragments<T, D>(qn, qbase + ((size_t)nx.b * p.num_q_heads + (size_t)nx.g * G) * D,
                                    G, lane);
             L_next = p.context_lens[nx.b];
+            slot_next = p.slot_mapping[nx.b];
         }
-        const int st = warp + kConsumerWarps * (k % Lay::kPerWarp);
-        bool ok = mbar_wait(&full_bar[st], (k / Lay::kPerWarp) & 1);
+        const int st = k % R;
+        bool ok = mbar_wait(&full[st], (k / R) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
             return;
         }
-        uint8_t* ktile = smem + st * Lay::kStageBytes;
+        const int blk = sblk[st];
+        uint8_t* ktile = ring + st * Lay::kStageBytes;
         uint8_t* vtile = ktile + Lay::kTileBytes;
         if (kFp8) {
+            // E4M3 -> T into the warp's 16-bit tiles; the stage is free again
             convert_fp8_tiles<T>(ktile, conv, conv + Lay::kTile16Bytes, lane);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[st]);
+            if (k + R < count) issue(k + R);
             ktile = conv;
             vtile = conv + Lay::kTile16Bytes;
         }
-        if (t == (L - 1) / kTileTokens) {
+        if (slot >= 0 && t == (L - 1) / kTileTokens) {
             // the segment's last tile holds its new token (position L - 1)
-            const int64_t slot = p.slot_mapping[b];
-            if (slot >= 0) {
-                const int pos = L - 1;
-                const int64_t blk = p.block_tables[(size_t)b * p.max_blocks_per_seq +
-                                                   pos / p.block_size];
-                if (slot == blk * p.block_size + pos % p.block_size && blk >= 0 &&
-                    blk < p.num_blocks) {
-                    const int c = lane & 15;
-                    if (c < D / 8) {
-                        const bool is_k = lane < 16;
-                        put_tile_chunk(is_k ? ktile : vtile, pos % kTileTokens, c,
-                                       balanced_new_token<T, D, kFp8>(p, b, g, slot, c, is_k));
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                } else if (lane == 0 && g == 0) {
-                    flag_error(p.err, PA_DEVERR_BAD_SLOT);
+            const int pos = L - 1;
+            if (slot == (int64_t)blk * p.block_size + pos % p.block_size && blk >= 0 &&
+                blk < p.num_blocks) {
+                const int c = lane & 15;
+                if (c < D / 8) {
+                    const bool is_k = lane < 16;
+                    put_tile_chunk(is_k ? ktile : vtile, pos % kTileTokens, c,
+                                   balanced_new_token<T, D, kFp8>(p, b, g, slot, c, is_k));
                 }
+                fence_proxy_async_smem();    // before a later TMA write of the stage
+                __syncwarp();
+            } else if (lane == 0 && g == 0) {
+                flag_error(p.err, PA_DEVERR_BAD_SLOT);
             }
         }
         attend_tile<T, D>(ts, qb, ktile, vtile, t * kTileTokens, L, p.scale_log2, lane);
         __syncwarp();
-        if (!kFp8 && lane == 0) mbar_arrive(&empty_bar[st]);
+        if (!kFp8 && k + R < count) issue(k + R);
 
         if (piece_end) {
             ts.reduce_row_sums();
@@ -496,12 +514,12 @@ cudaError_t launch_balanced_t(const CUtensorMap& tmk, const CUtensorMap& tmv,
     cudaError_t e = launch_with_pdl(balanced_plan_kernel<T, D>, dim3(1), dim3(kPlanThreads), 0,
                                     stream, p);
     if (e != cudaSuccess) return e;
-    const int smem = BalancedLayout<D, kFp8>::kDynamicSmem;
+    const int smem = StreamLayout<D, kFp8>::kDynamicSmem;
     e = cudaFuncSetAttribute(balanced_step_kernel<T, D, kFp8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_with_pdl(balanced_step_kernel<T, D, kFp8>, dim3(num_ctas),
-                           dim3(kDecodeThreads), smem, stream, tmk, tmv, p);
+                           dim3(kStreamWarps * 32), smem, stream, tmk, tmv, p);
 }
 
 cudaError_t launch_balanced(int dtype, int head_dim, bool fp8, const CUtensorMap& tmk,

@@ -34,6 +34,22 @@ static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of consu
 constexpr int kStagesFp8 = 2 * kStages;
 constexpr int kMinCtasPerSmFp8 = 4;
 static_assert(kStagesFp8 % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
+// Work-balanced step (balanced.cu): every warp of a CTA streams its own tile
+// range and issues its own TMA loads into a private ring of
+// PA_STREAM_RING_KIB KiB (16-bit tiles; an FP8 warp keeps 8 KiB of it for its
+// 16-bit copy of the tile).
+#ifndef PA_STREAM_WARPS
+#define PA_STREAM_WARPS 4
+#endif
+#ifndef PA_STREAM_RING_KIB
+#define PA_STREAM_RING_KIB 24
+#endif
+#ifndef PA_STREAM_CTAS_PER_SM
+#define PA_STREAM_CTAS_PER_SM 2
+#endif
+constexpr int kStreamWarps = PA_STREAM_WARPS;
+constexpr int kStreamRingBytes = PA_STREAM_RING_KIB * 1024;
+constexpr int kStreamCtasPerSm = PA_STREAM_CTAS_PER_SM;
 constexpr int kMaxGroup = 8;         // query heads per KV head served by one CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
