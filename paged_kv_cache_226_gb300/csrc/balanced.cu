@@ -100,10 +100,10 @@ __global__ void __launch_bounds__(kPlanThreads)
             if ((long long)prefix[mid] > key) hi = mid; else lo = mid + 1;
         }
         const int b = lo - 1;
-        const int T = prefix[b + 1] - prefix[b];
+        const int Tb = prefix[b + 1] - prefix[b];
         const long long off = x - (long long)p.num_kv_heads * prefix[b];
-        const int g = (int)(off / T);
-        starts[ws] = make_int4(b, g, (int)(off - (long long)g * T), T);
+        const int g = (int)(off / Tb);
+        starts[ws] = make_int4(b, g, (int)(off - (long long)g * Tb), Tb);
     }
 }
 
@@ -147,7 +147,7 @@ struct StreamLayout {
     static constexpr int kTileBytes = kHalves * kBox16Bytes;       // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kTile16Bytes = (D / kBoxElems) * kBox16Bytes;
-    static constexpr int kConvBytes = kFp8 ? 2 * kTile16Bytes : 0;  // FP8: 16-bit K, V copy
+    static constexpr int kConvBytes = 0;     // FP8 codes go from the stage to registers
     static constexpr int kRing = (kStreamRingBytes - kConvBytes) / kStageBytes;  // stages
     static constexpr int kWarpBytes = kRing * kStageBytes + kConvBytes;
     static constexpr int kDynamicSmem = kStreamWarps * kWarpBytes + 1024;
@@ -156,7 +156,8 @@ struct StreamLayout {
 };
 
 // Writes the fused step's new token (chunk c of K or V, head g) into the
-// cache and returns it in the 16-bit compute type; FP8 caches get E4M3 codes.
+// cache and returns it as staged data: the 16-bit values, or for an FP8
+// cache its eight E4M3 codes in .x and .y.
 template <typename T, int D, bool kFp8>
 __device__ __forceinline__ uint4 balanced_new_token(const BalancedParams& p, int b, int g,
                                                     int64_t slot, int c, bool is_k) {
@@ -171,17 +172,16 @@ __device__ __forceinline__ uint4 balanced_new_token(const BalancedParams& p, int
     const float sc = is_k ? p.k_scale : p.v_scale;
     const uint32_t w[4] = {val.x, val.y, val.z, val.w};
     uint16_t q[4];
-    uint32_t back[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float2 f = Mma<T>::unpack(w[j]);
         q[j] = f32x2_to_e4m3x2(__fdiv_rn(f.y, sc), __fdiv_rn(f.x, sc));
-        back[j] = e4m3x2_to<T>(q[j]);
     }
     uint8_t* cache = reinterpret_cast<uint8_t*>(is_k ? p.k_cache : p.v_cache);
-    *reinterpret_cast<uint2*>(cache + dst + 8 * c) =
-        make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
-    return make_uint4(back[0], back[1], back[2], back[3]);
+    const uint2 codes = make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16),
+                                   (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+    *reinterpret_cast<uint2*>(cache + dst + 8 * c) = codes;
+    return make_uint4(codes.x, codes.y, 0u, 0u);
 }
 
 // Log-sum-exp merge of the np pieces (records wfirst + j + z) of segment z by
@@ -288,7 +288,6 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t* ring = smem + warp * Lay::kWarpBytes;
-    uint8_t* conv = ring + R * Lay::kStageBytes;
     uint64_t* full = full_bar[warp];
     int* sblk = stage_blk[warp];
 
@@ -381,8 +380,17 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
     TileState<D> ts;
     // the first piece's query rows, length and new-token slot; later pieces'
     // are prefetched during the last tile of the piece before
-    load_q_fragments<T, D>(qn, qbase + ((size_t)cur.b * p.num_q_heads + (size_t)cur.g * G) * D, G,
-                           lane);
+    // (FP8: fp16 fragments of q / 2^s in the FP8 dim order, s kept beside them)
+    auto load_q = [&](uint32_t (&dst)[D / 16][2], const T* src) -> int {
+        if constexpr (kFp8) {
+            return load_q_fragments_fp8<T>(dst, src, G, lane);
+        } else {
+            load_q_fragments<T, D>(dst, src, G, lane);
+            return 0;
+        }
+    };
+    int sq_next = load_q(qn, qbase + ((size_t)cur.b * p.num_q_heads + (size_t)cur.g * G) * D);
+    float scale_log2 = p.scale_log2;
     int L_next = p.context_lens[cur.b];
     int64_t slot_next = p.slot_mapping[cur.b];
     int L = 0;
@@ -392,6 +400,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
         if (k == 0 || t == 0) {                          // a piece begins
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) qb[kk][0] = qn[kk][0], qb[kk][1] = qn[kk][1];
+            scale_log2 = p.scale_log2 * __int_as_float((127 + sq_next) << 23);
             L = L_next < 0 ? 0 : (L_next > max_ctx ? max_ctx : L_next);
             slot = slot_next;
             ts.reset();
@@ -400,8 +409,7 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
         if (piece_end && k + 1 < count) {
             TileCursor nx = cur;
             nx.advance(1, prefix, B, Hkv);
-            load_q_fragments<T, D>(qn, qbase + ((size_t)nx.b * p.num_q_heads + (size_t)nx.g * G) * D,
-                                   G, lane);
+            sq_next = load_q(qn, qbase + ((size_t)nx.b * p.num_q_heads + (size_t)nx.g * G) * D);
             L_next = p.context_lens[nx.b];
             slot_next = p.slot_mapping[nx.b];
         }
@@ -414,24 +422,20 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
         const int blk = sblk[st];
         uint8_t* ktile = ring + st * Lay::kStageBytes;
         uint8_t* vtile = ktile + Lay::kTileBytes;
-        if (kFp8) {
-            // E4M3 -> T into the warp's 16-bit tiles; the stage is free again
-            convert_fp8_tiles<T>(ktile, conv, conv + Lay::kTile16Bytes, lane);
-            __syncwarp();
-            if (k + R < count) issue(k + R);
-            ktile = conv;
-            vtile = conv + Lay::kTile16Bytes;
-        }
         if (slot >= 0 && t == (L - 1) / kTileTokens) {
             // the segment's last tile holds its new token (position L - 1)
             const int pos = L - 1;
             if (slot == (int64_t)blk * p.block_size + pos % p.block_size && blk >= 0 &&
                 blk < p.num_blocks) {
                 const int c = lane & 15;
-                if (c < D / 8) {
-                    const bool is_k = lane < 16;
+                const bool is_k = lane < 16;
+                if constexpr (kFp8) {
+                    const uint4 cv = balanced_new_token<T, D, true>(p, b, g, slot, c, is_k);
+                    put_code_chunk(is_k ? ktile : vtile, pos % kTileTokens, c,
+                                   make_uint2(cv.x, cv.y));
+                } else if (c < D / 8) {
                     put_tile_chunk(is_k ? ktile : vtile, pos % kTileTokens, c,
-                                   balanced_new_token<T, D, kFp8>(p, b, g, slot, c, is_k));
+                                   balanced_new_token<T, D, false>(p, b, g, slot, c, is_k));
                 }
                 fence_proxy_async_smem();    // before a later TMA write of the stage
                 __syncwarp();
@@ -439,9 +443,16 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
                 flag_error(p.err, PA_DEVERR_BAD_SLOT);
             }
         }
-        attend_tile<T, D>(ts, qb, ktile, vtile, t * kTileTokens, L, p.scale_log2, lane);
-        __syncwarp();
-        if (!kFp8 && k + R < count) issue(k + R);
+        if constexpr (kFp8) {
+            attend_tile_fp8(ts, qb, ktile, vtile, t * kTileTokens, L, scale_log2, lane, [&] {
+                __syncwarp();                // the codes are in registers: refill the stage
+                if (k + R < count) issue(k + R);
+            });
+        } else {
+            attend_tile<T, D>(ts, qb, ktile, vtile, t * kTileTokens, L, scale_log2, lane);
+            __syncwarp();
+            if (k + R < count) issue(k + R);
+        }
 
         if (piece_end) {
             ts.reduce_row_sums();
@@ -456,14 +467,15 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
                 T* out = reinterpret_cast<T*>(p.out) + qh0 * D;
 #pragma unroll
                 for (int n = 0; n < D / 16; ++n) {
-                    const int d = 16 * n + r8;
+                    int d_lo = 16 * n + r8, d_hi = d_lo + 8;
+                    if constexpr (kFp8) fp8_dims(n, r8, d_lo, d_hi);
                     if (hA < G) {
-                        out[hA * D + d] = from_float<T>(ts.acc[n][0] * iA);
-                        out[hA * D + d + 8] = from_float<T>(ts.acc[n][2] * iA);
+                        out[hA * D + d_lo] = from_float<T>(ts.acc[n][0] * iA);
+                        out[hA * D + d_hi] = from_float<T>(ts.acc[n][2] * iA);
                     }
                     if (hB < G) {
-                        out[hB * D + d] = from_float<T>(ts.acc[n][1] * iB);
-                        out[hB * D + d + 8] = from_float<T>(ts.acc[n][3] * iB);
+                        out[hB * D + d_lo] = from_float<T>(ts.acc[n][1] * iB);
+                        out[hB * D + d_hi] = from_float<T>(ts.acc[n][3] * iB);
                     }
                 }
             } else {
@@ -472,14 +484,15 @@ __global__ void __launch_bounds__(kStreamWarps * 32, kStreamCtasPerSm)
                 float* ro = p.rec_o + rec * G * D;
 #pragma unroll
                 for (int n = 0; n < D / 16; ++n) {
-                    const int d = 16 * n + r8;
+                    int d_lo = 16 * n + r8, d_hi = d_lo + 8;
+                    if constexpr (kFp8) fp8_dims(n, r8, d_lo, d_hi);
                     if (hA < G) {
-                        ro[hA * D + d] = ts.acc[n][0] * iA;
-                        ro[hA * D + d + 8] = ts.acc[n][2] * iA;
+                        ro[hA * D + d_lo] = ts.acc[n][0] * iA;
+                        ro[hA * D + d_hi] = ts.acc[n][2] * iA;
                     }
                     if (hB < G) {
-                        ro[hB * D + d] = ts.acc[n][1] * iB;
-                        ro[hB * D + d + 8] = ts.acc[n][3] * iB;
+                        ro[hB * D + d_lo] = ts.acc[n][1] * iB;
+                        ro[hB * D + d_hi] = ts.acc[n][3] * iB;
                     }
                 }
                 if (r8 == 0) {

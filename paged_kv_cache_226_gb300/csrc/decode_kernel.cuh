@@ -42,8 +42,7 @@ struct DecodeLayout {
     // 16-bit compute tiles (the layout ldmatrix reads): D/64 boxes of [16][128 B]
     static constexpr int kHalves16 = D / kBoxElems;
     static constexpr int kTile16Bytes = kHalves16 * kBoxBytes;
-    // FP8: each consumer warp converts its staged tile into private K and V tiles
-    static constexpr int kConvBytes = kFp8 ? kConsumerWarps * 2 * kTile16Bytes : 0;
+    static constexpr int kConvBytes = 0;     // FP8 codes go from the stage to registers
     // merge area: per warp, O[8][D] then m_used[8], l[8], m_true[8]
     static constexpr int kMergeFloatsPerWarp = kMaxGroup * D + 3 * kMaxGroup;
     static constexpr int kMergeBytes = kConsumerWarps * kMergeFloatsPerWarp * 4;
@@ -53,10 +52,10 @@ struct DecodeLayout {
 };
 
 // The fused step's new token, 16-byte chunk c (8 dims) of its K (is_k) or V
-// row for KV head g: written to the cache at new_slot and returned in the
-// 16-bit compute type.  With an FP8 cache the chunk is quantised first
-// (E4M3 of x / scale, the quotient in fp32) and the returned values are the
-// codes' values -- what attention reads back from the cache.
+// row for KV head g: written to the cache at new_slot and returned as staged
+// data: the 16-bit values, or with an FP8 cache the chunk's eight E4M3 codes
+// (of x / scale, the quotient in fp32) in .x and .y -- what attention reads
+// back from the cache.
 template <typename T, int D, bool kFp8>
 __device__ __forceinline__ uint4 new_token_chunk(const DecodeParams& p, int b, int g,
                                                  int64_t new_slot, int c, bool is_k) {
@@ -72,17 +71,16 @@ __device__ __forceinline__ uint4 new_token_chunk(const DecodeParams& p, int b, i
     const float sc = is_k ? p.k_scale : p.v_scale;
     const uint32_t w[4] = {val.x, val.y, val.z, val.w};
     uint16_t q[4];
-    uint32_t back[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float2 f = Mma<T>::unpack(w[j]);
         q[j] = f32x2_to_e4m3x2(__fdiv_rn(f.y, sc), __fdiv_rn(f.x, sc));
-        back[j] = e4m3x2_to<T>(q[j]);
     }
     uint8_t* cache = reinterpret_cast<uint8_t*>(is_k ? p.k_cache : p.v_cache);
-    *reinterpret_cast<uint2*>(cache + dst + 8 * c) =
-        make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16));
-    return make_uint4(back[0], back[1], back[2], back[3]);
+    const uint2 codes = make_uint2((uint32_t)q[0] | ((uint32_t)q[1] << 16),
+                                   (uint32_t)q[2] | ((uint32_t)q[3] << 16));
+    *reinterpret_cast<uint2*>(cache + dst + 8 * c) = codes;
+    return make_uint4(codes.x, codes.y, 0u, 0u);
 }
 
 template <typename T, int D, int kMode, bool kFp8 = false>
@@ -219,8 +217,16 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
     const int hA = 2 * c4, hB = 2 * c4 + 1;      // this thread's two heads
 
     uint32_t qb[kKSteps][2];
-    load_q_fragments<T, D>(qb, reinterpret_cast<const T*>(p.q) +
-                                   ((size_t)b * p.num_q_heads + (size_t)g * G) * D, G, lane);
+    float scale_log2 = p.scale_log2;
+    {
+        const T* qg = reinterpret_cast<const T*>(p.q) + ((size_t)b * p.num_q_heads + (size_t)g * G) * D;
+        if constexpr (kFp8) {
+            const int sq = load_q_fragments_fp8<T>(qb, qg, G, lane);   // q / 2^sq in fp16
+            scale_log2 *= __int_as_float((127 + sq) << 23);
+        } else {
+            load_q_fragments<T, D>(qb, qg, G, lane);
+        }
+    }
     TileState<D> ts;
     ts.reset();
 
@@ -254,32 +260,39 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         }
         uint8_t* ktile = smem + st * Lay::kStageBytes;
         uint8_t* vtile = ktile + Lay::kTileBytes;
-        if (kFp8) {
-            // E4M3 -> T into this warp's private tiles, then free the stage
-            uint8_t* conv = smem + Lay::kPipeBytes + warp * 2 * Lay::kTile16Bytes;
-            convert_fp8_tiles<T>(ktile, conv, conv + Lay::kTile16Bytes, lane);
+        if constexpr (kFp8) {
+            if (kMode == kModeStep && it == new_tile) {
+                // lanes 0-15: 8-code chunks of K, lanes 16-31: of V, into the staged codes
+                const int c = lane & 15;
+                const bool is_k = lane < 16;
+                const uint4 cv = new_token_chunk<T, D, true>(p, b, g, new_slot, c, is_k);
+                put_code_chunk(is_k ? ktile : vtile, (L - 1) % kTileTokens, c,
+                               make_uint2(cv.x, cv.y));
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            attend_tile_fp8(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
+                            scale_log2, lane, [&] {
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&empty_bar[st]);
+                            });
+        } else {
+            if (kMode == kModeStep && it == new_tile) {
+                // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V
+                const int c = lane & 15;
+                if (c < D / 8) {
+                    const bool is_k = lane < 16;
+                    put_tile_chunk(is_k ? ktile : vtile, (L - 1) % kTileTokens, c,
+                                   new_token_chunk<T, D, false>(p, b, g, new_slot, c, is_k));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            attend_tile<T, D>(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
+                              scale_log2, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[st]);
-            ktile = conv;
-            vtile = conv + Lay::kTile16Bytes;
         }
-
-        if (kMode == kModeStep && it == new_tile) {
-            // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V (in the 16-bit tile)
-            const int c = lane & 15;
-            if (c < D / 8) {
-                const bool is_k = lane < 16;
-                put_tile_chunk(is_k ? ktile : vtile, (L - 1) % kTileTokens, c,
-                               new_token_chunk<T, D, kFp8>(p, b, g, new_slot, c, is_k));
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-
-        attend_tile<T, D>(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
-                          p.scale_log2, lane);
-        __syncwarp();
-        if (!kFp8 && lane == 0) mbar_arrive(&empty_bar[st]);
     }
 
     if (kMode == kModeStep && new_slot >= 0 && new_tile < 0 && warp == 0) {
@@ -298,14 +311,15 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         float* wo = mrg + warp * Lay::kMergeFloatsPerWarp;
 #pragma unroll
         for (int n = 0; n < kKSteps; ++n) {
-            const int d = 16 * n + r8;
+            int d_lo = 16 * n + r8, d_hi = d_lo + 8;        // rows r8, r8 + 8 of slab n
+            if constexpr (kFp8) fp8_dims(n, r8, d_lo, d_hi);
             if (hA < G) {
-                wo[hA * D + d] = ts.acc[n][0];
-                wo[hA * D + d + 8] = ts.acc[n][2];
+                wo[hA * D + d_lo] = ts.acc[n][0];
+                wo[hA * D + d_hi] = ts.acc[n][2];
             }
             if (hB < G) {
-                wo[hB * D + d] = ts.acc[n][1];
-                wo[hB * D + d + 8] = ts.acc[n][3];
+                wo[hB * D + d_lo] = ts.acc[n][1];
+                wo[hB * D + d_hi] = ts.acc[n][3];
             }
         }
         if (r8 == 0) {

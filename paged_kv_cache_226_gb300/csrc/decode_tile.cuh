@@ -67,32 +67,183 @@ __device__ __forceinline__ void load_q_fragments(uint32_t (&qb)[D / 16][2], cons
     }
 }
 
-// E4M3 tile pair (K then V, each one [16][128 B] box of codes for D = 128)
-// -> the 16-bit layout above; warp-cooperative, exact.
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) tiles, D = 128: the staged tile is one box of [16 tokens][128 B]
+// codes per K and per V (128 B swizzle), and the products run in fp16 straight
+// from registers.  E4M3 codes are exact in fp16, so the staged values enter the
+// tensor cores unchanged; q is brought to fp16 once per warp (see
+// load_q_fragments_fp8) and P is rounded to fp16 once.
+//
+// The contraction and output orders are permuted so that every lane reads
+// whole 16-byte chunks:
+//   S^T = K q^T: in k-step kk, lane (r8, c4)'s four k positions (2c4, 2c4+1,
+//     2c4+8, 2c4+9) stand for dims 32 c4 + 4 kk + (0, 1, 2, 3): the lane reads
+//     bytes [32 c4, 32 c4 + 32) of token rows r8 and r8 + 8, and q is loaded
+//     with the same order.
+//   O^T += V^T P^T: slab n's rows r8 and r8 + 8 stand for dims 16 r8 + 2n and
+//     16 r8 + 2n + 1, so the lane reads bytes [16 r8, 16 r8 + 16) of token rows
+//     2c4, 2c4+1, 2c4+8, 2c4+9 and pairs bytes of two tokens with prmt.
+// Accumulator slab n of a lane therefore holds dims 16 r8 + 2n (c0, c1) and
+// 16 r8 + 2n + 1 (c2, c3); fp8_dims() gives them to the epilogues.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fp8_dims(int n, int r8, int& d_lo, int& d_hi) {
+    d_lo = 16 * r8 + 2 * n;
+    d_hi = d_lo + 1;
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
+    return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// q of the group as fp16 B fragments in the FP8 dim order, scaled by 2^-s so
+// that fp16 holds it (s = 0 for an fp16 q; a bf16 q above 2^15 in magnitude
+// gets the smallest s that brings it below); returns s.  Rows >= G are zero.
 template <typename T>
-__device__ __forceinline__ void convert_fp8_tiles(const uint8_t* src, uint8_t* dst_k,
-                                                  uint8_t* dst_v, int lane) {
+__device__ __forceinline__ int load_q_fragments_fp8(uint32_t (&qb)[8][2], const T* q_group, int G,
+                                                    int lane) {
+    const int r8 = lane >> 2, c4 = lane & 3;
+    const bool valid = r8 < G;
+    const uint4* src = reinterpret_cast<const uint4*>(q_group + (valid ? r8 : 0) * 128 + 32 * c4);
+    uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int u = lane + 32 * i;
-        const int kv = u >> 7, r = (u >> 3) & 15, c = u & 7;   // c: 16 dims 16c..16c+15
-        const uint4 raw = *reinterpret_cast<const uint4*>(
-            src + kv * kBox16Bytes + r * 128 + ((c ^ (r & 7)) << 4));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t h[8];
+    for (int i = 0; i < 4; ++i) {
+        const uint4 v = valid ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+        w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+    }
+    if constexpr (std::is_same<T, __half>::value) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            h[2 * j] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] & 0xffffu));
-            h[2 * j + 1] = e4m3x2_to<T>(static_cast<uint16_t>(w[j] >> 16));
+        for (int kk = 0; kk < 8; ++kk) qb[kk][0] = w[2 * kk], qb[kk][1] = w[2 * kk + 1];
+        return 0;
+    } else {
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float2 f = Mma<T>::unpack(w[i]);
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
         }
-        uint8_t* d = (kv ? dst_v : dst_k) + (c >> 2) * kBox16Bytes + r * 128;
-        const int j0 = 2 * (c & 3);
-        // lanes of the upper half of a row store their odd chunk first, so
-        // that each store instruction of 8 lanes covers 8 distinct bank groups
-        const int first = (c >> 2) ? 1 : 0;
-        const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]), hi = make_uint4(h[4], h[5], h[6], h[7]);
-        *reinterpret_cast<uint4*>(d + (((j0 + first) ^ (r & 7)) << 4)) = first ? hi : lo;
-        *reinterpret_cast<uint4*>(d + (((j0 + 1 - first) ^ (r & 7)) << 4)) = first ? lo : hi;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        int e = 0;
+        (void)frexpf(mx, &e);                        // mx < 2^e
+        const int s = e > 15 ? e - 15 : 0;
+        const float f = __int_as_float((127 - s) << 23);   // 2^-s, exact
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float2 v = Mma<T>::unpack(w[2 * kk + j]);
+                qb[kk][j] = Mma<__half>::pack(v.x * f, v.y * f);
+            }
+        }
+        return s;
+    }
+}
+
+// Writes 8 codes (8 dims, chunk c of 16) into token row r of an FP8 tile.
+__device__ __forceinline__ void put_code_chunk(uint8_t* tile, int r, int c, uint2 codes) {
+    *reinterpret_cast<uint2*>(tile + r * 128 + (((c >> 1) ^ (r & 7)) << 4) + (c & 1) * 8) = codes;
+}
+
+// Attends one FP8 tile pair (tokens tok0 .. tok0+15, masked from t_end on).
+// release() runs once the warp has read the staged codes into registers, so
+// the stage can be refilled while the P V products run.
+template <typename Release>
+__device__ __forceinline__ void attend_tile_fp8(TileState<128>& s, const uint32_t (&qb)[8][2],
+                                                const uint8_t* ktile, const uint8_t* vtile,
+                                                int tok0, int t_end, float scale_log2, int lane,
+                                                Release&& release) {
+    using M = Mma<__half>;
+    const int r8 = lane >> 2, c4 = lane & 3;
+    // K: chunks 2c4, 2c4+1 of token rows r8 and r8 + 8 (same swizzle row phase)
+    uint4 klo[2], khi[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int off = (((2 * c4 + i) ^ r8) << 4);
+        klo[i] = lds128(ktile + r8 * 128 + off);
+        khi[i] = lds128(ktile + (r8 + 8) * 128 + off);
+    }
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t wl = word_of(klo[kk >> 2], kk & 3);
+        const uint32_t wh = word_of(khi[kk >> 2], kk & 3);
+        const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl & 0xffffu));
+        const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl >> 16));
+        const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh & 0xffffu));
+        const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh >> 16));
+        M::run(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+    }
+    // V: chunk r8 of token rows 2c4, 2c4+1, 2c4+8, 2c4+9; rows past the end are
+    // cleared (they may hold stale codes, NaN among them)
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = 2 * c4 + (i & 1) + 8 * (i >> 1);
+        v[i] = lds128(vtile + t * 128 + ((r8 ^ (t & 7)) << 4));
+        if (tok0 + t >= t_end) v[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    release();
+
+    const bool v_lo = tok0 + r8 < t_end, v_hi8 = tok0 + r8 + 8 < t_end;
+    const float x0 = v_lo ? sc[0] * scale_log2 : -INFINITY;
+    const float x1 = v_lo ? sc[1] * scale_log2 : -INFINITY;
+    const float x2 = v_hi8 ? sc[2] * scale_log2 : -INFINITY;
+    const float x3 = v_hi8 ? sc[3] * scale_log2 : -INFINITY;
+    float xa = fmaxf(x0, x2), xb = fmaxf(x1, x3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, o));
+    }
+    s.tA = fmaxf(s.tA, xa);
+    s.tB = fmaxf(s.tB, xb);
+    const bool raiseA = xa > s.mA + kRescaleThresholdLog2;
+    const bool raiseB = xb > s.mB + kRescaleThresholdLog2;
+    if (__any_sync(0xffffffffu, raiseA || raiseB)) {
+        const float nA = raiseA ? xa : s.mA, nB = raiseB ? xb : s.mB;
+        const float fA = ex2(s.mA - nA), fB = ex2(s.mB - nB);
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            s.acc[n][0] *= fA;
+            s.acc[n][1] *= fB;
+            s.acc[n][2] *= fA;
+            s.acc[n][3] *= fB;
+        }
+        s.lA *= fA;
+        s.lB *= fB;
+        s.mA = nA;
+        s.mB = nB;
+    }
+    const uint32_t p01 = M::pack(ex2(x0 - s.mA), ex2(x1 - s.mB));
+    const uint32_t p23 = M::pack(ex2(x2 - s.mA), ex2(x3 - s.mB));
+    {
+        const float2 u = M::unpack(p01), w = M::unpack(p23);
+        s.lA += u.x + w.x;
+        s.lB += u.y + w.y;
+    }
+    const uint32_t pb0 = movmatrix_trans(p01);
+    const uint32_t pb1 = movmatrix_trans(p23);
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+        const int j = n >> 1;
+        const uint32_t sel = (n & 1) ? 0x7362u : 0x5140u;   // bytes (2h, 2h+1) of two tokens
+        const uint32_t x01 = prmt(word_of(v[0], j), word_of(v[1], j), sel);
+        const uint32_t x23 = prmt(word_of(v[2], j), word_of(v[3], j), sel);
+        const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xffffu));
+        const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16));
+        const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 & 0xffffu));
+        const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 >> 16));
+        M::run(s.acc[n], a0, a1, a2, a3, pb0, pb1);
     }
 }
 

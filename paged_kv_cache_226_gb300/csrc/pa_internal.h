@@ -29,10 +29,14 @@ constexpr int kMinCtasPerSm = PA_DECODE_MIN_CTAS_PER_SM;
 // one warp, which waits on its phases in order; otherwise two warps would
 // share a stage and a parity wait could match a phase two laps old.
 static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
-// The FP8 cache halves the bytes of a tile, so its ring is twice as deep
-// (and the CTA keeps a 16-bit copy per warp): 4 CTAs per SM.
+// The FP8 cache halves the bytes of a tile, so its ring is twice as deep;
+// its warps build fragments from the staged codes in registers, and six
+// CTAs per SM (96 registers a thread) beat four or five on long contexts.
+#ifndef PA_DECODE_MIN_CTAS_PER_SM_FP8
+#define PA_DECODE_MIN_CTAS_PER_SM_FP8 6
+#endif
 constexpr int kStagesFp8 = 2 * kStages;
-constexpr int kMinCtasPerSmFp8 = 4;
+constexpr int kMinCtasPerSmFp8 = PA_DECODE_MIN_CTAS_PER_SM_FP8;
 static_assert(kStagesFp8 % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
 // Work-balanced step (balanced.cu): every warp of a CTA streams its own tile
 // range and issues its own TMA loads into a private ring of
