@@ -106,8 +106,10 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 // q of the group as fp16 B fragments in the FP8 dim order, scaled by 2^-s so
-// that fp16 holds it (s = 0 for an fp16 q; a bf16 q above 2^15 in magnitude
-// gets the smallest s that brings it below); returns s.  Rows >= G are zero.
+// that fp16 holds it; returns s.  An fp16 q is taken as it is (s = 0); a bf16
+// q is scaled so that the group's largest magnitude lands in [2^14, 2^15),
+// which keeps every value within fp16's range and its 11 significant bits
+// for all but values 2^-24 below the largest.  Rows >= G are zero.
 template <typename T>
 __device__ __forceinline__ int load_q_fragments_fp8(uint32_t (&qb)[8][2], const T* q_group, int G,
                                                     int lane) {
@@ -134,8 +136,8 @@ __device__ __forceinline__ int load_q_fragments_fp8(uint32_t (&qb)[8][2], const 
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         int e = 0;
-        (void)frexpf(mx, &e);                        // mx < 2^e
-        const int s = e > 15 ? e - 15 : 0;
+        (void)frexpf(mx, &e);                        // mx < 2^e (e = 0 for mx = 0)
+        const int s = min(100, max(-100, e - 15));
         const float f = __int_as_float((127 - s) << 23);   // 2^-s, exact
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {

@@ -109,6 +109,19 @@ def test_fp8_edge_lengths(dev, dtype, bs):
         _check_fp8(w, kc, vc, dev, partition_size=P)
 
 
+@pytest.mark.parametrize("log2_q", [17, -20, 0])
+def test_fp8_bf16_query_magnitudes(dev, log2_q):
+    """A bf16 query far above fp16's range (2^17) or far below its normal range
+    (2^-20), with the softmax scale compensating, attends like any other: the
+    FP8 path computes in fp16 and must bring q into range first."""
+    w, kc, vc = _fp8_case(params=dict(dtype="bf16", num_seqs=5, lens=[1, 33, 300, 700, 1500],
+                                      num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                      block_size=16), seed=23)
+    w.q = (w.q.float() * 2.0 ** log2_q).to(torch.bfloat16)
+    w.scale = w.scale * 2.0 ** -log2_q
+    _check_fp8(w, kc, vc, dev)
+
+
 def test_fp8_rejects_head_dim_64_and_bad_scales(dev):
     q = torch.zeros((1, 4, 64), dtype=torch.float16, device=dev)
     kc = torch.zeros((4, 16, 2, 64), dtype=torch.uint8, device=dev)
