@@ -248,6 +248,18 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
                const pa_shape* shp, void* stream);
 
 /*
+ * pa_prefill_mma: the same operation, arguments and errors as pa_prefill,
+ * always on the mma.sync kernel (16 query tokens per CTA, any group size and
+ * head_dim 64 or 128).  pa_prefill takes the tcgen05 kernel (128 query rows
+ * per CTA, accumulators in tensor memory) when head_dim is 128 and the group
+ * size Hq / Hkv is 1, 2, 4 or 8, and this one otherwise.
+ */
+int pa_prefill_mma(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, const int32_t* context_lens,
+                   const int32_t* query_start, float scale, int32_t max_query_len, void* out,
+                   const pa_shape* shp, void* stream);
+
+/*
  * pa_copy_blocks: copy whole physical blocks between two block pools.  For
  * each pair p < num_pairs of block_mapping (int64 [num_pairs][2], device):
  *   src = block_mapping[2p], dst = block_mapping[2p+1],

@@ -434,6 +434,48 @@ int decode_step_balanced(const void* q, const void* k, const void* v, const int6
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+int prefill_any(const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens,
+                const int32_t* query_start, float scale, int32_t max_query_len, void* out,
+                const pa_shape* shp, void* stream, bool mma_sync_only) {
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if (max_query_len < 0) return PA_ERR_INVALID_ARG;
+    if (shp->num_seqs == 0 || max_query_len == 0) return PA_OK;
+    if (!query_start || (reinterpret_cast<uintptr_t>(query_start) & 3u) || !out || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    const int64_t qtiles = (max_query_len + 15) / 16;
+    if (qtiles > 0x7fffffffll) return PA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv;
+    if ((st = encode_cache_map(&tmk, k_cache, shp, false)) != PA_OK) return st;
+    if ((st = encode_cache_map(&tmv, v_cache, shp, false)) != PA_OK) return st;
+    int* err = nullptr;
+    cudaError_t e = error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pa::PrefillParams p{};
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start = query_start;
+    p.err = err;
+    p.scale_log2 = scale * pa::kLog2e;
+    p.num_q_heads = shp->num_q_heads;
+    p.group = shp->num_q_heads / shp->num_kv_heads;
+    p.max_blocks_per_seq = shp->max_blocks_per_seq;
+    p.block_size = shp->block_size;
+    p.num_blocks = shp->num_blocks;
+    if (pa::prefill_tc_supported(shp->head_dim, p.group) && !mma_sync_only) {
+        e = pa::launch_prefill_tc(shp->dtype, tmk, tmv, p, max_query_len, shp->num_kv_heads,
+                                  shp->num_seqs, static_cast<cudaStream_t>(stream));
+    } else {
+        dim3 grid((unsigned)qtiles, shp->num_kv_heads, shp->num_seqs);
+        e = pa::launch_prefill(shp->dtype, shp->head_dim, tmk, tmv, p, grid,
+                               static_cast<cudaStream_t>(stream));
+    }
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -557,37 +599,16 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, const int32_t* context_lens,
                const int32_t* query_start, float scale, int32_t max_query_len, void* out,
                const pa_shape* shp, void* stream) {
-    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
-    if (st != PA_OK) return st;
-    if (max_query_len < 0) return PA_ERR_INVALID_ARG;
-    if (shp->num_seqs == 0 || max_query_len == 0) return PA_OK;
-    if (!query_start || (reinterpret_cast<uintptr_t>(query_start) & 3u) || !out || !aligned16(out))
-        return PA_ERR_INVALID_ARG;
-    const int64_t qtiles = (max_query_len + 15) / 16;
-    if (qtiles > 0x7fffffffll) return PA_ERR_UNSUPPORTED;
-    CUtensorMap tmk, tmv;
-    if ((st = encode_cache_map(&tmk, k_cache, shp, false)) != PA_OK) return st;
-    if ((st = encode_cache_map(&tmv, v_cache, shp, false)) != PA_OK) return st;
-    int* err = nullptr;
-    cudaError_t e = error_word(&err);
-    if (e != cudaSuccess) return cuda_fail(e);
-    pa::PrefillParams p{};
-    p.q = q;
-    p.out = out;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.query_start = query_start;
-    p.err = err;
-    p.scale_log2 = scale * pa::kLog2e;
-    p.num_q_heads = shp->num_q_heads;
-    p.group = shp->num_q_heads / shp->num_kv_heads;
-    p.max_blocks_per_seq = shp->max_blocks_per_seq;
-    p.block_size = shp->block_size;
-    p.num_blocks = shp->num_blocks;
-    dim3 grid((unsigned)qtiles, shp->num_kv_heads, shp->num_seqs);
-    e = pa::launch_prefill(shp->dtype, shp->head_dim, tmk, tmv, p, grid,
-                           static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+    return prefill_any(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                       max_query_len, out, shp, stream, false);
+}
+
+int pa_prefill_mma(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, const int32_t* context_lens,
+                   const int32_t* query_start, float scale, int32_t max_query_len, void* out,
+                   const pa_shape* shp, void* stream) {
+    return prefill_any(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                       max_query_len, out, shp, stream, true);
 }
 
 int pa_copy_blocks(const void* k_src, const void* v_src, int64_t src_num_blocks, void* k_dst,

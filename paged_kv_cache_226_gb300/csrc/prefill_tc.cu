@@ -1,0 +1,428 @@
+// Chunked-prefill attention on the fifth-generation tensor cores (tcgen05,
+// tensor-memory accumulators), head_dim 128 and GQA groups of 1, 2, 4 or 8.
+//
+// Sequence b holds L_b tokens, the last C_b of which are new; new token i
+// sits at position L_b - C_b + i and attends causally to positions 0..itself
+// (ta-paperlens page, prefill vs decode and the quadratic cost of prefill;
+// techfeed summary, chunked prefill).  One CTA serves 128 query rows: 128 / G
+// new tokens of one (sequence, KV head) times the G query heads that read
+// that KV head, so every K/V tile is read once for all of them.
+//
+// Per 128-key tile j (keys 128 j .. 128 j + 127 through the block table):
+//   S_j = Q K_j^T          128 x 128 x 128 into tensor memory (two buffers)
+//   P_j = 2^(S_j - m)      eight softmax warps, two threads per row, lazily
+//                          raised running max m (log2 units, threshold 2^8:
+//                          the accumulator is rescaled in tensor memory only
+//                          when a row's max grows by more than that)
+//   O  += P_j V_j          128 x 128 x 128, O in tensor memory; bf16 P as a
+//                          hi + lo pair of products
+// Warp roles: warp 0 streams K and V tiles (TMA, 16-token boxes of the paged
+// cache, two stages), lane 0 of warp 1 issues every MMA and commits it to
+// mbarriers, warps 2-9 run the softmax and the epilogue, two threads per row
+// (warps 2-5 keys / dims 0-63, warps 6-9 keys / dims 64-127, the pair
+// exchanging row maxima and sums through shared memory).  S_{j+1} is issued
+// before P_j is ready, and P_j is computed before P_{j-1} V_{j-1} has
+// finished, so only the store of P waits on the previous product.  Every
+// mbarrier wait gives up after 1 s and flags PA_DEVERR_WAIT_TIMEOUT; the
+// softmax warps then run their remaining iterations without waiting (so the
+// pair barriers always complete), and tensor memory is always released.
+#include "decode_tile.cuh"
+#include "tc_device.cuh"
+
+namespace pa {
+
+constexpr int kTcRows = 128;                 // query rows per CTA (tokens x heads)
+constexpr int kTcKeys = 128;                 // keys per K/V tile
+constexpr int kTcStages = 2;                 // K/V tile pairs in flight
+constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
+constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0, S1, O (+ spare)
+constexpr int kTcOperand = 32768;            // 128 rows x 2 halves x 128 B
+constexpr int kTcHalf = 16384;               // one 64-element half: 128 rows x 128 B
+
+template <bool kSplitP>
+struct TcLayout {
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTcOperand;
+    static constexpr int kV = kK + kTcStages * kTcOperand;
+    static constexpr int kP = kV + kTcStages * kTcOperand;       // P (bf16: hi), then lo
+    static constexpr int kBytes = kP + (kSplitP ? 2 : 1) * kTcOperand;
+    static constexpr int kDynamicSmem = kBytes + 1024;
+    // with the ~1.1 KB of static shared memory (barriers, pair exchange) this
+    // must stay within the 227 KB a CTA may hold
+    static_assert(kDynamicSmem + 1200 <= 232448, "shared memory over the per-CTA limit");
+};
+
+// Byte offset of 16-byte chunk c (elements 8c .. 8c+7 of 128) of row r in an
+// operand of two 64-element halves with the 128-byte swizzle.
+__device__ __forceinline__ int tc_chunk(int r, int c) {
+    return (c >> 3) * kTcHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v,
+                            const __grid_constant__ PrefillParams p) {
+    constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr bool kSplitP = kBf16;
+    using Lay = TcLayout<kSplitP>;
+    using M = Mma<T>;
+    __shared__ __align__(8) uint64_t k_full[kTcStages], v_full[kTcStages];
+    __shared__ __align__(8) uint64_t k_empty[kTcStages], v_empty[kTcStages];
+    __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full, o_done;
+    __shared__ uint32_t tmem_base;
+    __shared__ float pair_x[2][kTcRows];           // [half][row]: row maxima, then sums
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int qt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.group;
+    const int QT = kTcRows / G;                             // new tokens per CTA
+
+    grid_dependency_wait();
+    allow_dependent_launch();
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    int L = p.context_lens[b];
+    if (L < 0 || L > max_ctx) {
+        if (threadIdx.x == 0 && qt == 0 && g == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+        L = L < 0 ? 0 : max_ctx;
+    }
+    const int q0 = p.query_start[b];
+    int C = p.query_start[b + 1] - q0;
+    if (C > L) {
+        if (threadIdx.x == 0 && qt == 0 && g == 0) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+        C = L;
+    }
+    const int t0 = qt * QT;
+    if (t0 >= C) return;
+    const int rows = min(QT, C - t0);
+    const int last_pos = L - C + t0 + rows - 1;             // the CTA's last query position
+    const int n_tiles = last_pos / kTcKeys + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], kTcSoftmaxWarps);         // one arrival per softmax warp
+        }
+        mbar_init(&p_full, kTcSoftmaxWarps);
+        mbar_init(&o_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
+    if (warp >= 2) {
+        // Q rows as the K-major A operand: row r = (token r / G, head r % G);
+        // rows past the chunk are zero; each thread of the pair loads one half
+        const int r = (warp & 3) * 32 + lane, half = (warp - 2) >> 2;
+        const int t = r / G, h = r % G;
+        uint8_t* dq = smem + Lay::kQ;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const T*>(p.q) +
+            ((size_t)(q0 + t0 + min(t, rows - 1)) * p.num_q_heads + (size_t)g * G + h) * 128);
+#pragma unroll
+        for (int c = 8 * half; c < 8 * half + 8; ++c) {
+            const uint4 v = t < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dq + tc_chunk(r, c)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------
+        // producer: K and V tiles, 16-token boxes through the block table;
+        // boxes wholly past the context are not loaded.  K runs one tile
+        // ahead of V (K_j is free once S_j is computed, V_j only after P_j V_j):
+        // K_0, K_1, V_0, K_2, V_1, ...
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            prefetch_tensor_map(&tmap_k);
+            prefetch_tensor_map(&tmap_v);
+        }
+        const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
+        // boxes of tile j: this lane's block id and token offset for box `lane`
+        auto describe = [&](int j, int& nbox, int& blk, int& sub) {
+            const int key0 = j * kTcKeys;
+            nbox = min(8, (L - key0 + 15) / 16);
+            blk = 0, sub = 0;
+            if (lane < nbox) {
+                const int tok = key0 + 16 * lane;
+                blk = __ldg(table + tok / p.block_size);
+                sub = tok % p.block_size;
+            }
+        };
+        // one operand (K or V) of tile j into stage j % kTcStages
+        auto load = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, int kind_off,
+                        int j, int nbox, int blk, int sub) -> bool {
+            const int s = j % kTcStages;
+            bool ok = true;
+            if (lane == 0) {
+                if (j >= kTcStages && !mbar_wait(&empty[s], ((j / kTcStages) - 1) & 1)) {
+                    flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+                    ok = false;
+                } else {
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)nbox * 2u * kBox16Bytes);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) return false;
+            if (lane < nbox && (blk < 0 || blk >= p.num_blocks)) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+            uint8_t* dst = smem + kind_off + s * kTcOperand;
+            for (int i = 0; i < nbox; ++i) {
+                const int bi = __shfl_sync(0xffffffffu, blk, i);
+                const int si = __shfl_sync(0xffffffffu, sub, i);
+                if (lane == 0) {
+                    tma_load_4d(dst + i * kBox16Bytes, map, &full[s], 0, g, si, bi);
+                    tma_load_4d(dst + kTcHalf + i * kBox16Bytes, map, &full[s], kBoxElems, g, si, bi);
+                }
+            }
+            return true;
+        };
+        int nb_k = 0, blk_k = 0, sub_k = 0, nb_v = 0, blk_v = 0, sub_v = 0;
+        describe(0, nb_k, blk_k, sub_k);
+        bool ok = load(&tmap_k, k_full, k_empty, Lay::kK, 0, nb_k, blk_k, sub_k);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            nb_v = nb_k, blk_v = blk_k, sub_v = sub_k;        // V_j uses K_j's boxes
+            if (j + 1 < n_tiles) {
+                describe(j + 1, nb_k, blk_k, sub_k);
+                ok = load(&tmap_k, k_full, k_empty, Lay::kK, j + 1, nb_k, blk_k, sub_k);
+            }
+            if (ok) ok = load(&tmap_v, v_full, v_empty, Lay::kV, j, nb_v, blk_v, sub_v);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------
+        // MMA issuer: S_j, then P_{j-1} V_{j-1}
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, kBf16, false);
+            constexpr uint32_t kIdPV = idesc_f16(kTcRows, 128, kBf16, true);
+            const uint32_t aQ = smem_u32(smem + Lay::kQ);
+            bool ok = true;
+            for (int j = 0; j <= n_tiles && ok; ++j) {
+                if (j < n_tiles) {
+                    const int s = j % kTcStages, bb = j & 1;
+                    ok = mbar_wait(&k_full[s], (j / kTcStages) & 1);
+                    if (ok && j >= 2) ok = mbar_wait(&s_free[bb], ((j - 2) >> 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t aK = smem_u32(smem + Lay::kK + s * kTcOperand);
+                    const uint32_t dS = bb ? tS1 : tS0;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+                        mma_f16_ss(dS, smem_desc_sw128(aQ + off, 16, 1024),
+                                   smem_desc_sw128(aK + off, 16, 1024), kIdS, kk > 0);
+                    }
+                    mma_commit(&s_full[bb]);
+                    mma_commit(&k_empty[s]);                // S_j has read K_j
+                }
+                if (j >= 1) {
+                    const int jp = j - 1, s = jp % kTcStages;
+                    ok = mbar_wait(&p_full, jp & 1);
+                    if (ok) ok = mbar_wait(&v_full[s], (jp / kTcStages) & 1);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t aV = smem_u32(smem + Lay::kV + s * kTcOperand);
+#pragma unroll
+                    for (int part = 0; part < (kSplitP ? 2 : 1); ++part) {
+                        const uint32_t aP = smem_u32(smem + Lay::kP + part * kTcOperand);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t offP = (kk >> 2) * kTcHalf + (kk & 3) * 32;
+                            mma_f16_ss(tO, smem_desc_sw128(aP + offP, 16, 1024),
+                                       smem_desc_sw128(aV + kk * 16 * 128, kTcHalf, 1024), kIdPV,
+                                       jp > 0 || part > 0 || kk > 0);
+                        }
+                    }
+                    mma_commit(&o_done);
+                    mma_commit(&v_empty[s]);                // P_j V_j has read V_j
+                }
+            }
+            if (!ok) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // softmax and epilogue: this thread owns half `half` (64 keys of each
+        // tile, 64 output dims) of row r (tensor-memory lane r)
+        // ------------------------------------------------------------------
+        const int r = (warp & 3) * 32 + lane, half = (warp - 2) >> 2;
+        const int t = r / G, h = r % G;
+        const int pos = min(L - C + t0 + t, L - 1);
+        const uint32_t lane_addr = ((uint32_t)((warp & 3) * 32) << 16) + 64 * half;
+        constexpr int kHalfKeys = kTcKeys / 2;
+        float m = -INFINITY, l = 0.f;
+        bool failed = false;                 // a wait ran out: finish the loop without waiting
+        auto wait = [&](uint64_t* bar, uint32_t parity) {
+            if (!failed && !__all_sync(0xffffffffu, mbar_wait(bar, parity))) failed = true;
+        };
+        for (int j = 0; j < n_tiles; ++j) {
+            const int bb = j & 1, s = j % kTcStages;
+            wait(&s_full[bb], (j >> 1) & 1);
+            tc_fence_after_sync();
+            float x[kHalfKeys];
+            {
+                uint32_t v0[32], v1[32];
+                tmem_ld32((bb ? tS1 : tS0) + lane_addr, v0);
+                tmem_ld32((bb ? tS1 : tS0) + lane_addr + 32, v1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    x[k] = __uint_as_float(v0[k]);
+                    x[32 + k] = __uint_as_float(v1[k]);
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[bb]);
+            // causal mask, log2 units, the row max over both halves
+            const int key0 = j * kTcKeys + kHalfKeys * half;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kHalfKeys; ++k) {
+                x[k] = key0 + k <= pos ? x[k] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[k]);
+            }
+            pair_x[half][r] = mx;
+            asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
+            mx = fmaxf(mx, pair_x[half ^ 1][r]);
+            asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
+            // the reference max: raised only when the row max grows past 2^8
+            const bool need = j > 0 && mx > m + kRescaleThresholdLog2;
+            const float f = need ? ex2(m - mx) : 1.f;
+            if (j == 0 || need) m = mx;                     // key 0 is visible to every row
+            l *= f;
+            // P = 2^(x - m) in registers (before the previous product has finished)
+            uint32_t hi[kHalfKeys / 2], lo[kHalfKeys / 2];
+#pragma unroll
+            for (int e = 0; e < kHalfKeys / 2; ++e) {
+                const float p0 = ex2(x[2 * e] - m), p1 = ex2(x[2 * e + 1] - m);
+                hi[e] = M::pack(p0, p1);
+                const float2 u = M::unpack(hi[e]);
+                if (kSplitP) {
+                    lo[e] = M::pack(p0 - u.x, p1 - u.y);
+                    l += p0 + p1;
+                } else {
+                    lo[e] = 0u;
+                    l += u.x + u.y;
+                }
+            }
+            // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
+            if (j > 0) {
+                wait(&o_done, (j - 1) & 1);
+                tc_fence_after_sync();
+            }
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + lane_addr + 32 * c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+                    tmem_st32(tO + lane_addr + 32 * c, v);
+                }
+                tmem_wait_st();
+            }
+            // the last tile: V rows past the context may hold stale bits; clear them
+            if (j * kTcKeys + kTcKeys > L) {
+                wait(&v_full[s], (j / kTcStages) & 1);
+                if (j * kTcKeys + r >= L) {
+                    uint8_t* vd = smem + Lay::kV + s * kTcOperand;
+#pragma unroll
+                    for (int c = 8 * half; c < 8 * half + 8; ++c)
+                        *reinterpret_cast<uint4*>(vd + tc_chunk(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            // P as the K-major A operand of P V (this thread: chunks 8 half .. +7)
+            uint8_t* dp = smem + Lay::kP;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int cc = 8 * half + c;
+                *reinterpret_cast<uint4*>(dp + tc_chunk(r, cc)) =
+                    make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+                if (kSplitP)
+                    *reinterpret_cast<uint4*>(dp + kTcOperand + tc_chunk(r, cc)) =
+                        make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full);
+        }
+        // epilogue: O / l for the chunk's rows, l summed over the pair
+        wait(&o_done, (n_tiles - 1) & 1);
+        pair_x[half][r] = l;
+        asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
+        if (!failed) {
+            tc_fence_after_sync();
+            const float inv = 1.f / (l + pair_x[half ^ 1][r]);
+            T* out = reinterpret_cast<T*>(p.out) +
+                     ((size_t)(q0 + t0 + min(t, rows - 1)) * p.num_q_heads + (size_t)g * G + h) * 128 +
+                     64 * half;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tO + lane_addr + 32 * c, v);
+                tmem_wait_ld();
+                if (t < rows) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = M::pack(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                           __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+                        *reinterpret_cast<uint4*>(out + 32 * c + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+        }
+    }
+
+    // every role is done with tensor memory
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTcCols);
+    }
+}
+
+template <typename T>
+cudaError_t launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                const PrefillParams& p, dim3 grid, cudaStream_t stream) {
+    const int smem = TcLayout<std::is_same<T, __nv_bfloat16>::value>::kDynamicSmem;
+    cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_with_pdl(paged_prefill_tc_kernel<T>, grid, dim3(kTcThreads), smem, stream, tmk,
+                           tmv, p);
+}
+
+bool prefill_tc_supported(int head_dim, int group) {
+    return head_dim == 128 && (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const PrefillParams& p, int max_query_len, int num_kv_heads,
+                              int num_seqs, cudaStream_t stream) {
+    const int qt = kTcRows / p.group;
+    dim3 grid((unsigned)((max_query_len + qt - 1) / qt), num_kv_heads, num_seqs);
+    if (dtype == PA_BF16) return launch_prefill_tc_t<__nv_bfloat16>(tmk, tmv, p, grid, stream);
+    return launch_prefill_tc_t<__half>(tmk, tmv, p, grid, stream);
+}
+
+}  // namespace pa

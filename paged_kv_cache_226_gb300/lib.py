@@ -81,8 +81,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                     ctypes.c_size_t, V, S, V]
         lib.pa_decode_step_balanced.restype = ctypes.c_int
         lib.pa_decode_step_balanced_fp8.restype = ctypes.c_int
-        lib.pa_prefill.argtypes = [V, V, V, V, V, V, F, I32, V, S, V]
-        lib.pa_prefill.restype = ctypes.c_int
+        for fn in (lib.pa_prefill, lib.pa_prefill_mma):
+            fn.argtypes = [V, V, V, V, V, V, F, I32, V, S, V]
+            fn.restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [V, V, I64, V, V, I64, V, I64, S, V]
         lib.pa_copy_blocks.restype = ctypes.c_int
         lib.pa_decode_step.argtypes = [V, V, V, V, V, V, V, V, F, I32, I32, V, V, V, V, V, S, V]
@@ -520,9 +521,11 @@ def decode_step_balanced(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_
 
 
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
-            max_query_len: int, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+            max_query_len: int, out: Optional[torch.Tensor] = None,
+            kernel: str = "auto") -> torch.Tensor:
     """Chunked-prefill attention (pa_prefill): the last C_b tokens of each
-    sequence attend causally over its cache; q, out [total_tokens][Hq][D]."""
+    sequence attend causally over its cache; q, out [total_tokens][Hq][D].
+    kernel "mma" forces the mma.sync kernel (pa_prefill_mma)."""
     lib = load()
     dev = k_cache.device
     _need(q, "q", k_cache.dtype, dev)
@@ -537,7 +540,8 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale:
     out = torch.empty_like(q) if out is None else out
     _need(out, "out", q.dtype, dev)
     shp = make_shape(B, q.shape[1], k_cache, block_tables.shape[1])
-    _check("pa_prefill", lib.pa_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+    fn = lib.pa_prefill_mma if kernel == "mma" else lib.pa_prefill
+    _check("pa_prefill", fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                         _ptr(context_lens), _ptr(query_start), float(scale),
                                         int(max_query_len), _ptr(out), ctypes.byref(shp),
                                         _stream_handle(dev)))

@@ -1,6 +1,8 @@
 """GPU parity of pa_prefill (chunked-prefill attention over the paged cache):
 the chunk's K/V written with pa_reshape_and_cache, then causal attention of
-every new token against the fp64 reference, |gpu - ref| <= 2e-3 + 1e-2 |ref|."""
+every new token against the fp64 reference, |gpu - ref| <= 2e-3 + 1e-2 |ref|.
+Both kernels are checked: the tcgen05 one (head_dim 128, groups 1/2/4/8,
+what pa_prefill takes there) and the mma.sync one (pa_prefill_mma)."""
 import numpy as np
 import pytest
 import torch
@@ -24,34 +26,38 @@ def dev():
     return d
 
 
-def _check_prefill(w, dev):
+def _check_prefill(w, dev, kernel="auto"):
     d = {k: (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).to(dev)
          for k, v in dict(q=w.q, kn=w.k_new, vn=w.v_new, kc=w.k_cache, vc=w.v_cache,
                           bt=w.block_tables, cl=w.context_lens, qs=w.query_start,
                           sm=w.slot_mapping).items()}
     lib.reshape_and_cache(d["kn"], d["vn"], d["sm"], d["kc"], d["vc"])
     max_q = int(np.diff(w.query_start).max()) if w.num_seqs else 0
-    out = lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q)
+    out = lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q,
+                      kernel=kernel)
     kc, vc, _ = oracle.reshape_and_cache(pin.bits(w.k_new), pin.bits(w.v_new), w.slot_mapping,
                                          pin.bits(w.k_cache), pin.bits(w.v_cache), w.block_size)
     want = oracle.paged_prefill(pin.bits(w.q), kc, vc, w.block_tables, w.context_lens,
                                 w.query_start, w.scale, w.dtype)
     torch.cuda.synchronize(dev)
     assert np.array_equal(pin.bits(d["kc"].cpu()), kc)
-    err = assert_close(out.float().cpu().numpy(), want, f"{w.name} prefill")
+    err = assert_close(out.float().cpu().numpy(), want, f"{w.name} prefill ({kernel})")
     assert lib.read_device_errors(dev) == 0
     return err
 
 
+@pytest.mark.parametrize("kernel", ["auto", "mma"])
 @pytest.mark.parametrize("name", ["prefill_tiny", "prefill8b"])
-def test_named_prefill(dev, name):
-    _check_prefill(pin.build_prefill_workload(name), dev)
+def test_named_prefill(dev, name, kernel):
+    _check_prefill(pin.build_prefill_workload(name), dev, kernel)
 
 
 @pytest.mark.parametrize("dtype,hq,hkv,d,bs", [
     ("fp16", 8, 2, 64, 16), ("bf16", 32, 8, 128, 16), ("fp16", 64, 8, 128, 32),
-    ("bf16", 4, 4, 128, 16), ("fp16", 16, 8, 64, 32), ("bf16", 12, 2, 128, 16)])
-def test_prefill_shapes_and_ragged_chunks(dev, dtype, hq, hkv, d, bs):
+    ("bf16", 4, 4, 128, 16), ("fp16", 16, 8, 64, 32), ("bf16", 12, 2, 128, 16),
+    ("fp16", 16, 8, 128, 16)])
+@pytest.mark.parametrize("kernel", ["auto", "mma"])
+def test_prefill_shapes_and_ragged_chunks(dev, dtype, hq, hkv, d, bs, kernel):
     lens = [1, 15, 16, 17, 33, 100, 257, 700, 40]
     chunks = [1, 15, 1, 17, 16, 37, 257, 300, 0]
     w = pin.build_prefill_workload(params=dict(dtype=dtype, lens=lens, chunks=chunks,
@@ -72,3 +78,14 @@ def test_one_token_chunks_equal_decode(dev):
     dec = lib.decode(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], w.scale)
     assert_close(pre.float().cpu().numpy(), dec.float().cpu().numpy(), "prefill(1) vs decode",
                  atol=1e-3, rtol=5e-3)
+
+
+def test_prefill_long_chunks_many_tiles(dev):
+    """Chunks past 128 tokens and contexts of many 128-key tiles, with a
+    sequence whose chunk is its whole context (plain prefill)."""
+    w = pin.build_prefill_workload(params=dict(dtype="bf16", lens=[3000, 777, 1024, 129],
+                                               chunks=[700, 777, 1, 129], num_q_heads=32,
+                                               num_kv_heads=8, head_dim=128, block_size=32),
+                                   seed=41)
+    _check_prefill(w, dev)
+    _check_prefill(w, dev, "mma")
