@@ -465,7 +465,7 @@ int prefill_any(const void* q, const void* k_cache, const void* v_cache,
     p.max_blocks_per_seq = shp->max_blocks_per_seq;
     p.block_size = shp->block_size;
     p.num_blocks = shp->num_blocks;
-    if (pa::prefill_tc_supported(shp->head_dim, p.group) && !mma_sync_only) {
+    if (pa::prefill_tc_supported(shp->head_dim, p.group, scale) && !mma_sync_only) {
         e = pa::launch_prefill_tc(shp->dtype, tmk, tmv, p, max_query_len, shp->num_kv_heads,
                                   shp->num_seqs, static_cast<cudaStream_t>(stream));
     } else {

@@ -145,8 +145,9 @@ struct PrefillParams {
 cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap& tmk,
                            const CUtensorMap& tmv, const PrefillParams& p, dim3 grid,
                            cudaStream_t stream);
-// tcgen05 chunked prefill (prefill_tc.cu): head_dim 128, groups of 1, 2, 4, 8.
-bool prefill_tc_supported(int head_dim, int group);
+// tcgen05 chunked prefill (prefill_tc.cu): head_dim 128, groups of 1, 2, 4, 8,
+// a positive softmax scale.
+bool prefill_tc_supported(int head_dim, int group, float scale);
 cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tmk, const CUtensorMap& tmv,
                               const PrefillParams& p, int max_query_len, int num_kv_heads,
                               int num_seqs, cudaStream_t stream);

@@ -15,7 +15,8 @@
 //                          the accumulator is rescaled in tensor memory only
 //                          when a row's max grows by more than that)
 //   O  += P_j V_j          128 x 128 x 128, O in tensor memory; bf16 P as a
-//                          hi + lo pair of products
+//                          hi + lo pair of products (both cut from the fp32
+//                          bits, together exact to 2^-15)
 // Warp roles: warp 0 streams K and V tiles (TMA, 16-token boxes of the paged
 // cache, two stages), lane 0 of warp 1 issues every MMA and commits it to
 // mbarriers, warps 2-9 run the softmax and the epilogue, two threads per row
@@ -285,14 +286,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[bb]);
-            // causal mask, log2 units, the row max over both halves
+            // causal mask (only on tiles that reach past this row's position),
+            // log2 units, the row max over both halves (eight independent
+            // partial maxima and sums keep the dependency chains short)
             const int key0 = j * kTcKeys + kHalfKeys * half;
-            float mx = -INFINITY;
+            float pm[8];
 #pragma unroll
-            for (int k = 0; k < kHalfKeys; ++k) {
-                x[k] = key0 + k <= pos ? x[k] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[k]);
+            for (int i = 0; i < 8; ++i) pm[i] = -INFINITY;
+            if (key0 + kHalfKeys - 1 <= pos) {
+#pragma unroll
+                for (int k = 0; k < kHalfKeys; ++k) {
+                    x[k] *= p.scale_log2;
+                    pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kHalfKeys; ++k) {
+                    x[k] = key0 + k <= pos ? x[k] * p.scale_log2 : -INFINITY;
+                    pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+                }
             }
+            float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                             fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
             pair_x[half][r] = mx;
             asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
             mx = fmaxf(mx, pair_x[half ^ 1][r]);
@@ -301,22 +316,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool need = j > 0 && mx > m + kRescaleThresholdLog2;
             const float f = need ? ex2(m - mx) : 1.f;
             if (j == 0 || need) m = mx;                     // key 0 is visible to every row
-            l *= f;
             // P = 2^(x - m) in registers (before the previous product has finished)
             uint32_t hi[kHalfKeys / 2], lo[kHalfKeys / 2];
+            float ps[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ps[i] = 0.f;
 #pragma unroll
             for (int e = 0; e < kHalfKeys / 2; ++e) {
                 const float p0 = ex2(x[2 * e] - m), p1 = ex2(x[2 * e + 1] - m);
-                hi[e] = M::pack(p0, p1);
-                const float2 u = M::unpack(hi[e]);
                 if (kSplitP) {
-                    lo[e] = M::pack(p0 - u.x, p1 - u.y);
-                    l += p0 + p1;
+                    // bf16 hi = p with its low 16 bits cut off (exact in fp32), lo =
+                    // the remainder, also cut to bf16: hi + lo carries p to 2^-15,
+                    // with integer and fp32 adds only
+                    const float h0 = __uint_as_float(__float_as_uint(p0) & 0xffff0000u);
+                    const float h1 = __uint_as_float(__float_as_uint(p1) & 0xffff0000u);
+                    hi[e] = prmt(__float_as_uint(p0), __float_as_uint(p1), 0x7632u);
+                    lo[e] = prmt(__float_as_uint(p0 - h0), __float_as_uint(p1 - h1), 0x7632u);
+                    ps[e & 7] += p0 + p1;
                 } else {
+                    hi[e] = M::pack(p0, p1);
+                    const float2 u = M::unpack(hi[e]);
                     lo[e] = 0u;
-                    l += u.x + u.y;
+                    ps[e & 7] += u.x + u.y;
                 }
             }
+            l = l * f + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
             // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
             if (j > 0) {
                 wait(&o_done, (j - 1) & 1);
@@ -412,8 +436,8 @@ cudaError_t launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv,
                            tmv, p);
 }
 
-bool prefill_tc_supported(int head_dim, int group) {
-    return head_dim == 128 && (group == 1 || group == 2 || group == 4 || group == 8);
+bool prefill_tc_supported(int head_dim, int group, float scale) {
+    return head_dim == 128 && (group == 1 || group == 2 || group == 4 || group == 8) && scale > 0.f;
 }
 
 cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tmk, const CUtensorMap& tmv,
