@@ -9,24 +9,28 @@
 // that KV head, so every K/V tile is read once for all of them.
 //
 // Per 128-key tile j (keys 128 j .. 128 j + 127 through the block table):
-//   S_j = Q K_j^T          128 x 128 x 128 into tensor memory (two buffers)
-//   P_j = 2^(S_j - m)      eight softmax warps, two threads per row, lazily
-//                          raised running max m (log2 units, threshold 2^8:
-//                          the accumulator is rescaled in tensor memory only
-//                          when a row's max grows by more than that)
-//   O  += P_j V_j          128 x 128 x 128, O in tensor memory; bf16 P as a
-//                          hi + lo pair of products (both cut from the fp32
-//                          bits, together exact to 2^-15)
-// Warp roles: warp 0 streams K and V tiles (TMA, 16-token boxes of the paged
-// cache, two stages), lane 0 of warp 1 issues every MMA and commits it to
-// mbarriers, warps 2-9 run the softmax and the epilogue, two threads per row
-// (warps 2-5 keys / dims 0-63, warps 6-9 keys / dims 64-127, the pair
-// exchanging row maxima and sums through shared memory).  S_{j+1} is issued
-// before P_j is ready, and P_j is computed before P_{j-1} V_{j-1} has
-// finished, so only the store of P waits on the previous product.  Every
-// mbarrier wait gives up after 1 s and flags PA_DEVERR_WAIT_TIMEOUT; the
-// softmax warps then run their remaining iterations without waiting (so the
-// pair barriers always complete), and tensor memory is always released.
+//   S_j = Q K_j^T          128 x 128 x 128 into tensor memory (two buffers),
+//                          Q and K from shared memory
+//   P_j = 2^(S_j - m)      sixteen softmax warps, four threads per row (32
+//                          keys each, row maxima and sums exchanged through
+//                          shared memory), a lazily raised running max m (log2
+//                          units, threshold 2^8: the accumulator is rescaled
+//                          in tensor memory only when a row's max grows by
+//                          more than that); P goes to tensor memory (bf16: a
+//                          hi and a lo part cut from the fp32 bits, together
+//                          exact to 2^-15)
+//   O  += P_j V_j          128 x 128 x 128, P read from tensor memory, V from
+//                          its TMA-staged [key][dim] tile (MN-major), O in
+//                          tensor memory
+// Warp roles: warp 0 streams K (three stages) and V (two stages) tiles with
+// TMA, 16-token boxes of the paged cache, K two tiles ahead of V; lane 0 of
+// warp 1 issues every MMA and commits it to mbarriers; warps 2-17 run the
+// softmax and the epilogue.  S_{j+1} is issued before P_j is ready, and P_j
+// is computed before P_{j-1} V_{j-1} has finished, so only the store of P
+// waits on the previous product.  Every mbarrier wait gives up after 1 s and
+// flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
+// iterations without waiting (so their barriers always complete), and tensor
+// memory is always released.
 #include "decode_tile.cuh"
 #include "tc_device.cuh"
 
@@ -34,24 +38,26 @@ namespace pa {
 
 constexpr int kTcRows = 128;                 // query rows per CTA (tokens x heads)
 constexpr int kTcKeys = 128;                 // keys per K/V tile
-constexpr int kTcStages = 2;                 // K/V tile pairs in flight
-constexpr int kTcSoftmaxWarps = 8;
+constexpr int kTcKStages = 3;                // K tiles in flight
+constexpr int kTcVStages = 2;                // V tiles in flight
+constexpr int kTcPerRow = 4;                 // softmax threads per query row
+constexpr int kTcRowKeys = 128 / kTcPerRow;   // keys (and output dims) of one thread
+constexpr int kTcSoftmaxWarps = 4 * kTcPerRow;
+
 constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
-constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0, S1, O (+ spare)
+constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0, S1, O, P
 constexpr int kTcOperand = 32768;            // 128 rows x 2 halves x 128 B
 constexpr int kTcHalf = 16384;               // one 64-element half: 128 rows x 128 B
 
-template <bool kSplitP>
 struct TcLayout {
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kTcOperand;
-    static constexpr int kV = kK + kTcStages * kTcOperand;
-    static constexpr int kP = kV + kTcStages * kTcOperand;       // P (bf16: hi), then lo
-    static constexpr int kBytes = kP + (kSplitP ? 2 : 1) * kTcOperand;
+    static constexpr int kV = kK + kTcKStages * kTcOperand;
+    static constexpr int kBytes = kV + kTcVStages * kTcOperand;
     static constexpr int kDynamicSmem = kBytes + 1024;
-    // with the ~1.1 KB of static shared memory (barriers, pair exchange) this
+    // with the ~6.2 KB of static shared memory (barriers, row exchange) this
     // must stay within the 227 KB a CTA may hold
-    static_assert(kDynamicSmem + 1200 <= 232448, "shared memory over the per-CTA limit");
+    static_assert(kDynamicSmem + 6400 <= 232448, "shared memory over the per-CTA limit");
 };
 
 // Byte offset of 16-byte chunk c (elements 8c .. 8c+7 of 128) of row r in an
@@ -67,13 +73,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const __grid_constant__ PrefillParams p) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr bool kSplitP = kBf16;
-    using Lay = TcLayout<kSplitP>;
+    using Lay = TcLayout;
     using M = Mma<T>;
-    __shared__ __align__(8) uint64_t k_full[kTcStages], v_full[kTcStages];
-    __shared__ __align__(8) uint64_t k_empty[kTcStages], v_empty[kTcStages];
+    __shared__ __align__(8) uint64_t k_full[kTcKStages], k_empty[kTcKStages];
+    __shared__ __align__(8) uint64_t v_full[kTcVStages], v_empty[kTcVStages];
+    __shared__ float xchg[3][kTcPerRow][kTcRows];   // row maxima (two sets by tile parity), sums
     __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full, o_done;
     __shared__ uint32_t tmem_base;
-    __shared__ float pair_x[2][kTcRows];           // [half][row]: row maxima, then sums
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -103,10 +109,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_tiles = last_pos / kTcKeys + 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kTcKStages; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
             mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kTcVStages; ++s) {
+            mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -120,15 +128,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
     if (warp >= 2) {
         // Q rows as the K-major A operand: row r = (token r / G, head r % G);
-        // rows past the chunk are zero; each thread of the pair loads one half
-        const int r = (warp & 3) * 32 + lane, half = (warp - 2) >> 2;
+        // rows past the chunk are zero; each of the row's threads loads a quarter
+        const int r = (warp & 3) * 32 + lane, part = (warp - 2) >> 2;
         const int t = r / G, h = r % G;
         uint8_t* dq = smem + Lay::kQ;
         const uint4* src = reinterpret_cast<const uint4*>(
             reinterpret_cast<const T*>(p.q) +
             ((size_t)(q0 + t0 + min(t, rows - 1)) * p.num_q_heads + (size_t)g * G + h) * 128);
 #pragma unroll
-        for (int c = 8 * half; c < 8 * half + 8; ++c) {
+        for (int c = 4 * part; c < 4 * part + 4; ++c) {
             const uint4 v = t < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(dq + tc_chunk(r, c)) = v;
         }
@@ -139,13 +147,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base;
     const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
+    const uint32_t tP = tmem + 384;                         // P: hi [384, 448), lo [448, 512)
 
     if (warp == 0) {
         // ------------------------------------------------------------------
         // producer: K and V tiles, 16-token boxes through the block table;
-        // boxes wholly past the context are not loaded.  K runs one tile
-        // ahead of V (K_j is free once S_j is computed, V_j only after P_j V_j):
-        // K_0, K_1, V_0, K_2, V_1, ...
+        // boxes wholly past the context are not loaded.  K (three stages) runs
+        // two tiles ahead of V (two stages): K_j is free once S_j is computed,
+        // V_j only after P_j V_j: K_0, K_1, K_2, V_0, K_3, V_1, ...
         // ------------------------------------------------------------------
         if (lane == 0) {
             prefetch_tensor_map(&tmap_k);
@@ -163,13 +172,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 sub = tok % p.block_size;
             }
         };
-        // one operand (K or V) of tile j into stage j % kTcStages
+        // one operand (K or V) of tile j into stage j % stages
         auto load = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, int kind_off,
-                        int j, int nbox, int blk, int sub) -> bool {
-            const int s = j % kTcStages;
+                        int stages, int j) -> bool {
+            int nbox, blk, sub;
+            describe(j, nbox, blk, sub);
+            const int s = j % stages;
             bool ok = true;
             if (lane == 0) {
-                if (j >= kTcStages && !mbar_wait(&empty[s], ((j / kTcStages) - 1) & 1)) {
+                if (j >= stages && !mbar_wait(&empty[s], ((j / stages) - 1) & 1)) {
                     flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
                     ok = false;
                 } else {
@@ -190,16 +201,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return true;
         };
-        int nb_k = 0, blk_k = 0, sub_k = 0, nb_v = 0, blk_v = 0, sub_v = 0;
-        describe(0, nb_k, blk_k, sub_k);
-        bool ok = load(&tmap_k, k_full, k_empty, Lay::kK, 0, nb_k, blk_k, sub_k);
+        bool ok = load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, 0);
+        if (ok && n_tiles > 1) ok = load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, 1);
         for (int j = 0; j < n_tiles && ok; ++j) {
-            nb_v = nb_k, blk_v = blk_k, sub_v = sub_k;        // V_j uses K_j's boxes
-            if (j + 1 < n_tiles) {
-                describe(j + 1, nb_k, blk_k, sub_k);
-                ok = load(&tmap_k, k_full, k_empty, Lay::kK, j + 1, nb_k, blk_k, sub_k);
-            }
-            if (ok) ok = load(&tmap_v, v_full, v_empty, Lay::kV, j, nb_v, blk_v, sub_v);
+            if (j + 2 < n_tiles) ok = load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j + 2);
+            if (ok) ok = load(&tmap_v, v_full, v_empty, Lay::kV, kTcVStages, j);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
@@ -212,8 +218,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int j = 0; j <= n_tiles && ok; ++j) {
                 if (j < n_tiles) {
-                    const int s = j % kTcStages, bb = j & 1;
-                    ok = mbar_wait(&k_full[s], (j / kTcStages) & 1);
+                    const int s = j % kTcKStages, bb = j & 1;
+                    ok = mbar_wait(&k_full[s], (j / kTcKStages) & 1);
                     if (ok && j >= 2) ok = mbar_wait(&s_free[bb], ((j - 2) >> 1) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -229,22 +235,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_commit(&k_empty[s]);                // S_j has read K_j
                 }
                 if (j >= 1) {
-                    const int jp = j - 1, s = jp % kTcStages;
+                    const int jp = j - 1, s = jp % kTcVStages;
                     ok = mbar_wait(&p_full, jp & 1);
-                    if (ok) ok = mbar_wait(&v_full[s], (jp / kTcStages) & 1);
+                    if (ok) ok = mbar_wait(&v_full[s], (jp / kTcVStages) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t aV = smem_u32(smem + Lay::kV + s * kTcOperand);
 #pragma unroll
                     for (int part = 0; part < (kSplitP ? 2 : 1); ++part) {
-                        const uint32_t aP = smem_u32(smem + Lay::kP + part * kTcOperand);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t offP = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-                            mma_f16_ss(tO, smem_desc_sw128(aP + offP, 16, 1024),
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_f16_ts(tO, tP + 64 * part + 8 * kk,
                                        smem_desc_sw128(aV + kk * 16 * 128, kTcHalf, 1024), kIdPV,
                                        jp > 0 || part > 0 || kk > 0);
-                        }
                     }
                     mma_commit(&o_done);
                     mma_commit(&v_empty[s]);                // P_j V_j has read V_j
@@ -254,75 +257,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ------------------------------------------------------------------
-        // softmax and epilogue: this thread owns half `half` (64 keys of each
-        // tile, 64 output dims) of row r (tensor-memory lane r)
+        // softmax and epilogue: this thread owns quarter `part` (32 keys of each
+        // tile, 32 output dims) of row r (tensor-memory lane r); the row's four
+        // threads exchange maxima and sums through tensor-memory columns
         // ------------------------------------------------------------------
-        const int r = (warp & 3) * 32 + lane, half = (warp - 2) >> 2;
+        const int r = (warp & 3) * 32 + lane, part = (warp - 2) >> 2;
         const int t = r / G, h = r % G;
         const int pos = min(L - C + t0 + t, L - 1);
-        const uint32_t lane_addr = ((uint32_t)((warp & 3) * 32) << 16) + 64 * half;
-        constexpr int kHalfKeys = kTcKeys / 2;
+        const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t my_cols = lane_addr + kTcRowKeys * part;
         float m = -INFINITY, l = 0.f;
         bool failed = false;                 // a wait ran out: finish the loop without waiting
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             if (!failed && !__all_sync(0xffffffffu, mbar_wait(bar, parity))) failed = true;
         };
+        // the four threads' values of this row, through shared set `set`
+        auto exchange = [&](int set, float v) {
+            xchg[set][part][r] = v;
+            asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
+            return make_float4(xchg[set][0][r], xchg[set][1][r], xchg[set][2][r], xchg[set][3][r]);
+        };
         for (int j = 0; j < n_tiles; ++j) {
-            const int bb = j & 1, s = j % kTcStages;
+            const int bb = j & 1, s = j % kTcVStages;
             wait(&s_full[bb], (j >> 1) & 1);
             tc_fence_after_sync();
-            float x[kHalfKeys];
+            float x[kTcRowKeys];
             {
-                uint32_t v0[32], v1[32];
-                tmem_ld32((bb ? tS1 : tS0) + lane_addr, v0);
-                tmem_ld32((bb ? tS1 : tS0) + lane_addr + 32, v1);
+                uint32_t v0[32];
+                tmem_ld32((bb ? tS1 : tS0) + my_cols, v0);
                 tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    x[k] = __uint_as_float(v0[k]);
-                    x[32 + k] = __uint_as_float(v1[k]);
-                }
+                for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(v0[k]);
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_free[bb]);
             // causal mask (only on tiles that reach past this row's position),
-            // log2 units, the row max over both halves (eight independent
+            // log2 units, the row max over the four threads (eight independent
             // partial maxima and sums keep the dependency chains short)
-            const int key0 = j * kTcKeys + kHalfKeys * half;
+            const int key0 = j * kTcKeys + kTcRowKeys * part;
             float pm[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) pm[i] = -INFINITY;
-            if (key0 + kHalfKeys - 1 <= pos) {
+            if (key0 + kTcRowKeys - 1 <= pos) {
 #pragma unroll
-                for (int k = 0; k < kHalfKeys; ++k) {
+                for (int k = 0; k < kTcRowKeys; ++k) {
                     x[k] *= p.scale_log2;
                     pm[k & 7] = fmaxf(pm[k & 7], x[k]);
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < kHalfKeys; ++k) {
+                for (int k = 0; k < kTcRowKeys; ++k) {
                     x[k] = key0 + k <= pos ? x[k] * p.scale_log2 : -INFINITY;
                     pm[k & 7] = fmaxf(pm[k & 7], x[k]);
                 }
             }
             float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                              fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-            pair_x[half][r] = mx;
-            asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
-            mx = fmaxf(mx, pair_x[half ^ 1][r]);
-            asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
+            {
+                // two column sets by tile parity: a set is rewritten only after
+                // every thread has passed the next tile's barrier
+                const float4 e4 = exchange(bb, mx);
+                mx = fmaxf(fmaxf(e4.x, e4.y), fmaxf(e4.z, e4.w));
+            }
             // the reference max: raised only when the row max grows past 2^8
             const bool need = j > 0 && mx > m + kRescaleThresholdLog2;
             const float f = need ? ex2(m - mx) : 1.f;
             if (j == 0 || need) m = mx;                     // key 0 is visible to every row
             // P = 2^(x - m) in registers (before the previous product has finished)
-            uint32_t hi[kHalfKeys / 2], lo[kHalfKeys / 2];
+            uint32_t hi[kTcRowKeys / 2], lo[kTcRowKeys / 2];
             float ps[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) ps[i] = 0.f;
 #pragma unroll
-            for (int e = 0; e < kHalfKeys / 2; ++e) {
+            for (int e = 0; e < kTcRowKeys / 2; ++e) {
                 const float p0 = ex2(x[2 * e] - m), p1 = ex2(x[2 * e + 1] - m);
                 if (kSplitP) {
                     // bf16 hi = p with its low 16 bits cut off (exact in fp32), lo =
@@ -347,68 +355,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after_sync();
             }
             if (__any_sync(0xffffffffu, need)) {
+                uint32_t v[32];
+                tmem_ld32(tO + my_cols, v);
+                tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tO + lane_addr + 32 * c, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
-                    tmem_st32(tO + lane_addr + 32 * c, v);
-                }
+                for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * f);
+                tmem_st32(tO + my_cols, v);
                 tmem_wait_st();
             }
             // the last tile: V rows past the context may hold stale bits; clear them
             if (j * kTcKeys + kTcKeys > L) {
-                wait(&v_full[s], (j / kTcStages) & 1);
+                wait(&v_full[s], (j / kTcVStages) & 1);
                 if (j * kTcKeys + r >= L) {
                     uint8_t* vd = smem + Lay::kV + s * kTcOperand;
 #pragma unroll
-                    for (int c = 8 * half; c < 8 * half + 8; ++c)
+                    for (int c = 4 * part; c < 4 * part + 4; ++c)
                         *reinterpret_cast<uint4*>(vd + tc_chunk(r, c)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // P as the K-major A operand of P V (this thread: chunks 8 half .. +7)
-            uint8_t* dp = smem + Lay::kP;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const int cc = 8 * half + c;
-                *reinterpret_cast<uint4*>(dp + tc_chunk(r, cc)) =
-                    make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-                if (kSplitP)
-                    *reinterpret_cast<uint4*>(dp + kTcOperand + tc_chunk(r, cc)) =
-                        make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-            }
-            fence_proxy_async_smem();
+            // P into tensor memory as the A operand of P V: keys 2c, 2c+1 in
+            // column c of [384, 448) (bf16: lo parts in [448, 512)); this
+            // thread's 32 keys are 16 columns at 16 part
+            tmem_st16(tP + lane_addr + 16 * part, hi);
+            if (kSplitP) tmem_st16(tP + lane_addr + 64 + 16 * part, lo);
+            tmem_wait_st();
+            fence_proxy_async_smem();                       // the cleared V rows
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full);
         }
-        // epilogue: O / l for the chunk's rows, l summed over the pair
+        // epilogue: O / l for the chunk's rows, l summed over the row's threads
         wait(&o_done, (n_tiles - 1) & 1);
-        pair_x[half][r] = l;
-        asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
+        tc_fence_after_sync();
+        const float4 l4 = exchange(2, l);
         if (!failed) {
-            tc_fence_after_sync();
-            const float inv = 1.f / (l + pair_x[half ^ 1][r]);
+            const float inv = 1.f / ((l4.x + l4.y) + (l4.z + l4.w));
             T* out = reinterpret_cast<T*>(p.out) +
                      ((size_t)(q0 + t0 + min(t, rows - 1)) * p.num_q_heads + (size_t)g * G + h) * 128 +
-                     64 * half;
+                     kTcRowKeys * part;
+            uint32_t v[32];
+            tmem_ld32(tO + my_cols, v);
+            tmem_wait_ld();
+            if (t < rows) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tO + lane_addr + 32 * c, v);
-                tmem_wait_ld();
-                if (t < rows) {
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            w[e] = M::pack(__uint_as_float(v[8 * q + 2 * e]) * inv,
-                                           __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
-                        *reinterpret_cast<uint4*>(out + 32 * c + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = M::pack(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                       __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+                    *reinterpret_cast<uint4*>(out + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
         } else if (lane == 0) {
@@ -428,7 +424,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <typename T>
 cudaError_t launch_prefill_tc_t(const CUtensorMap& tmk, const CUtensorMap& tmv,
                                 const PrefillParams& p, dim3 grid, cudaStream_t stream) {
-    const int smem = TcLayout<std::is_same<T, __nv_bfloat16>::value>::kDynamicSmem;
+    const int smem = TcLayout::kDynamicSmem;
     cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
