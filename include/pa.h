@@ -252,7 +252,8 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
  * always on the mma.sync kernel (16 query tokens per CTA, any group size and
  * head_dim 64 or 128).  pa_prefill takes the tcgen05 kernel (128 query rows
  * per CTA, accumulators in tensor memory) when head_dim is 128, the group
- * size Hq / Hkv is 1, 2, 4 or 8 and scale > 0, and this one otherwise.
+ * size G = Hq / Hkv is 1, 2, 4 or 8, scale > 0 and max_query_len >= 128 / G
+ * (a chunk can fill its 128 rows), and this one otherwise.
  */
 int pa_prefill_mma(const void* q, const void* k_cache, const void* v_cache,
                    const int32_t* block_tables, const int32_t* context_lens,

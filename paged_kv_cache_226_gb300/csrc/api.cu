@@ -465,7 +465,9 @@ int prefill_any(const void* q, const void* k_cache, const void* v_cache,
     p.max_blocks_per_seq = shp->max_blocks_per_seq;
     p.block_size = shp->block_size;
     p.num_blocks = shp->num_blocks;
-    if (pa::prefill_tc_supported(shp->head_dim, p.group, scale) && !mma_sync_only) {
+    // the tcgen05 kernel's 128-row tiles pay off once a chunk can fill one
+    if (pa::prefill_tc_supported(shp->head_dim, p.group, scale) && !mma_sync_only &&
+        max_query_len >= 128 / p.group) {
         e = pa::launch_prefill_tc(shp->dtype, tmk, tmv, p, max_query_len, shp->num_kv_heads,
                                   shp->num_seqs, static_cast<cudaStream_t>(stream));
     } else {
