@@ -13,6 +13,7 @@ import re
 import threading
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -618,6 +619,35 @@ def read_device_errors(device: Optional[torch.device] = None) -> int:
         _check("pa_read_device_errors",
                lib.pa_read_device_errors(ctypes.byref(flags), _stream_handle(dev)))
     return int(flags.value)
+
+
+class InputStaging:
+    """A layer-step's host inputs (q, new K/V, slots, tables, lengths) as views
+    into one pinned host buffer and one device buffer, each view 256-byte
+    aligned, so a step uploads all of them with a single host-to-device copy.
+
+    ``specs`` maps names to (shape, dtype); ``h[name]`` / ``d[name]`` are the
+    host and device views.  Fill the host views, call ``upload()`` (on the
+    current stream), and hand the device views to the kernels.
+    """
+
+    def __init__(self, specs: dict, device: torch.device):
+        offsets, total = {}, 0
+        for name, (shape, dtype) in specs.items():
+            nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            offsets[name] = (total, nbytes, tuple(shape), dtype)
+            total += (nbytes + 255) // 256 * 256
+        self.nbytes = total
+        self.host = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(total, dtype=torch.uint8, device=device)
+        self.h, self.d = {}, {}
+        for name, (off, nbytes, shape, dtype) in offsets.items():
+            self.h[name] = self.host[off:off + nbytes].view(dtype).view(shape)
+            self.d[name] = self.dev[off:off + nbytes].view(dtype).view(shape)
+
+    def upload(self) -> None:
+        """All inputs host -> device in one asynchronous copy on the current stream."""
+        self.dev.copy_(self.host, non_blocking=True)
 
 
 class StepPlan:
