@@ -10,5 +10,5 @@ from .lib import (  # noqa: F401
     decode_step_balanced, load, prefill,
     num_partitions,
     paged_attention,
-    StepPlan, read_device_errors, reduce, reshape_and_cache, split_workspace,
+    StepPlan, InputStaging, read_device_errors, reduce, reshape_and_cache, split_workspace,
 )
