@@ -35,7 +35,10 @@ static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of consu
 #ifndef PA_DECODE_MIN_CTAS_PER_SM_FP8
 #define PA_DECODE_MIN_CTAS_PER_SM_FP8 6
 #endif
-constexpr int kStagesFp8 = 2 * kStages;
+#ifndef PA_DECODE_STAGES_FP8
+#define PA_DECODE_STAGES_FP8 (2 * PA_DECODE_STAGES)
+#endif
+constexpr int kStagesFp8 = PA_DECODE_STAGES_FP8;
 constexpr int kMinCtasPerSmFp8 = PA_DECODE_MIN_CTAS_PER_SM_FP8;
 static_assert(kStagesFp8 % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
 // Work-balanced step (balanced.cu): every warp of a CTA streams its own tile
