@@ -89,3 +89,33 @@ def test_prefill_long_chunks_many_tiles(dev):
                                    seed=41)
     _check_prefill(w, dev)
     _check_prefill(w, dev, "mma")
+
+
+@pytest.mark.parametrize("kernel", ["auto", "mma"])
+@pytest.mark.parametrize("dtype,bs", [("bf16", 16), ("fp16", 32)])
+def test_prefill_stale_nan_outside_the_contexts(dev, dtype, bs, kernel):
+    """Slots past each context's end (inside its last block) and every block no
+    table reaches hold NaN bits; neither kernel may let them into the result."""
+    w = pin.build_prefill_workload(params=dict(dtype=dtype, lens=[5, 130, 300, 1000],
+                                               chunks=[5, 130, 44, 300], num_q_heads=32,
+                                               num_kv_heads=8, head_dim=128, block_size=bs),
+                                   seed=53)
+    nan = 0x7fc0 if dtype == "bf16" else 0x7e00
+    kc, vc = pin.bits(w.k_cache).copy(), pin.bits(w.v_cache).copy()
+    used = set()
+    for b in range(w.num_seqs):
+        L = int(w.context_lens[b])
+        nblk = -(-L // bs)
+        used.update(int(x) for x in w.block_tables[b, :nblk])
+        last = w.block_tables[b, nblk - 1]
+        off = (L - 1) % bs + 1
+        kc[last, off:] = nan
+        vc[last, off:] = nan
+    for blk in range(w.num_blocks):
+        if blk not in used:
+            kc[blk] = nan
+            vc[blk] = nan
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    w.k_cache = torch.from_numpy(kc.view(np.int16)).view(tdt)
+    w.v_cache = torch.from_numpy(vc.view(np.int16)).view(tdt)
+    _check_prefill(w, dev, kernel)
