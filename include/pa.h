@@ -261,6 +261,18 @@ int pa_prefill_mma(const void* q, const void* k_cache, const void* v_cache,
                    const pa_shape* shp, void* stream);
 
 /*
+ * pa_copy_async: copy nbytes from src to dst with a short kernel on the
+ * stream (SM loads and stores, not a copy-engine transfer).  For a
+ * layer-step's small transfers: dst and src may each be device memory or
+ * pinned host memory (reached through unified addressing), both 16-byte
+ * aligned, nbytes a multiple of 16; the buffers must not overlap.  The launch
+ * takes part in programmatic dependent launch like the step kernels, so an
+ * upload, a step and a read-back chain without gaps.  No counterpart in the
+ * pages: it is the transport of the step's inputs and output.
+ */
+int pa_copy_async(void* dst, const void* src, size_t nbytes, void* stream);
+
+/*
  * pa_copy_blocks: copy whole physical blocks between two block pools.  For
  * each pair p < num_pairs of block_mapping (int64 [num_pairs][2], device):
  *   src = block_mapping[2p], dst = block_mapping[2p+1],

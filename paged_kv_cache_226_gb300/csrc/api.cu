@@ -613,6 +613,14 @@ int pa_prefill_mma(const void* q, const void* k_cache, const void* v_cache,
                        max_query_len, out, shp, stream, true);
 }
 
+int pa_copy_async(void* dst, const void* src, size_t nbytes, void* stream) {
+    if (nbytes == 0) return PA_OK;
+    if (!dst || !src || !aligned16(dst) || !aligned16(src) || (nbytes & 15u))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = pa::launch_copy16(dst, src, nbytes / 16, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 int pa_copy_blocks(const void* k_src, const void* v_src, int64_t src_num_blocks, void* k_dst,
                    void* v_dst, int64_t dst_num_blocks, const int64_t* block_mapping,
                    int64_t num_pairs, const pa_shape* shp, void* stream) {

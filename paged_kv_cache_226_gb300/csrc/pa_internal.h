@@ -148,6 +148,9 @@ struct PrefillParams {
 cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap& tmk,
                            const CUtensorMap& tmv, const PrefillParams& p, dim3 grid,
                            cudaStream_t stream);
+// Byte copies by SMs (stage_copy.cu): n16 16-byte vectors.
+cudaError_t launch_copy16(void* dst, const void* src, size_t n16, cudaStream_t stream);
+
 // tcgen05 chunked prefill (prefill_tc.cu): head_dim 128, groups of 1, 2, 4, 8,
 // a positive softmax scale.
 bool prefill_tc_supported(int head_dim, int group, float scale);

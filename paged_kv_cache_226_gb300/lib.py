@@ -82,6 +82,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                                     ctypes.c_size_t, V, S, V]
         lib.pa_decode_step_balanced.restype = ctypes.c_int
         lib.pa_decode_step_balanced_fp8.restype = ctypes.c_int
+        lib.pa_copy_async.argtypes = [V, V, ctypes.c_size_t, V]
+        lib.pa_copy_async.restype = ctypes.c_int
         for fn in (lib.pa_prefill, lib.pa_prefill_mma):
             fn.argtypes = [V, V, V, V, V, V, F, I32, V, S, V]
             fn.restype = ctypes.c_int
@@ -621,6 +623,25 @@ def read_device_errors(device: Optional[torch.device] = None) -> int:
     return int(flags.value)
 
 
+def copy_async(dst: torch.Tensor, src: torch.Tensor) -> torch.Tensor:
+    """dst <- src by a short kernel (pa_copy_async) on the current stream of
+    whichever side is on the device; either may be pinned host memory."""
+    if dst.numel() * dst.element_size() != src.numel() * src.element_size():
+        raise ValueError("copy_async needs equal byte sizes")
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("copy_async needs contiguous tensors")
+    for t in (dst, src):
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("copy_async: host tensors must be pinned")
+    dev = dst.device if dst.is_cuda else src.device
+    if not dev.type == "cuda":
+        raise ValueError("copy_async: one side must be on a CUDA device")
+    _check("pa_copy_async", load().pa_copy_async(_ptr(dst), _ptr(src),
+                                                 ctypes.c_size_t(dst.numel() * dst.element_size()),
+                                                 _stream_handle(dev)))
+    return dst
+
+
 class InputStaging:
     """A layer-step's host inputs (q, new K/V, slots, tables, lengths) as views
     into one pinned host buffer and one device buffer, each view 256-byte
@@ -645,9 +666,14 @@ class InputStaging:
             self.h[name] = self.host[off:off + nbytes].view(dtype).view(shape)
             self.d[name] = self.dev[off:off + nbytes].view(dtype).view(shape)
 
-    def upload(self) -> None:
-        """All inputs host -> device in one asynchronous copy on the current stream."""
-        self.dev.copy_(self.host, non_blocking=True)
+    def upload(self, engine: str = "kernel") -> None:
+        """All inputs host -> device in one asynchronous copy on the current
+        stream: by a short kernel reading the pinned buffer (``"kernel"``,
+        pa_copy_async) or by the copy engine (``"dma"``)."""
+        if engine == "kernel":
+            copy_async(self.dev, self.host)
+        else:
+            self.dev.copy_(self.host, non_blocking=True)
 
 
 class StepPlan:
@@ -783,16 +809,29 @@ class StepPlan:
         self.reduce()
         return self.out
 
-    def capture_graph(self) -> "torch.cuda.CUDAGraph":
-        """Capture one step into a CUDA graph (replayed by ``replay``)."""
+    def capture_graph(self, before=None, after=None) -> "torch.cuda.CUDAGraph":
+        """Capture one step into a CUDA graph (replayed by ``replay``).
+
+        ``before`` / ``after`` are called inside the capture around the step,
+        e.g. ``InputStaging.upload`` and the copy of ``out`` to pinned host
+        memory, so that a replay uploads, computes and reads back in one
+        graph launch."""
         s = torch.cuda.Stream(self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
-        with torch.cuda.stream(s):
-            self()                                   # warm the lazy set-up outside capture
+        with torch.cuda.stream(s):                   # warm the lazy set-up outside capture,
+            if before is not None:                   # with the same inputs the graph sees
+                before()
+            self()
+            if after is not None:
+                after()
         torch.cuda.current_stream(self.device).wait_stream(s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
+            if before is not None:
+                before()
             self()
+            if after is not None:
+                after()
         self._graph = g
         return g
 

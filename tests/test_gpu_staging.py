@@ -17,7 +17,9 @@ def dev():
         pytest.skip("no CUDA device")
     build.build()
     lib.load()
-    return torch.device("cuda:0")
+    d = torch.device("cuda:0")
+    lib.read_device_errors(d)
+    return d
 
 
 def test_staged_step_matches_separate_tensors(dev):
@@ -51,3 +53,57 @@ def test_staged_step_matches_separate_tensors(dev):
     torch.cuda.synchronize(dev)
     assert torch.equal(staged.out, plain.out)
     assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+    assert lib.read_device_errors(dev) == 0
+
+
+def test_graph_with_upload_and_readback(dev):
+    """A step captured with its upload and read-back replays to the same output
+    after the host inputs change (new token rows written between replays)."""
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=6, lens=[3, 40, 77, 300, 512, 1000],
+                                       num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                       block_size=16), seed=37)
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    src = {k: (torch.from_numpy(getattr(w, k)) if isinstance(getattr(w, k), np.ndarray)
+               else getattr(w, k)) for k in names}
+    stage = lib.InputStaging({k: (tuple(t.shape), t.dtype) for k, t in src.items()}, dev)
+    for k, t in src.items():
+        stage.h[k].copy_(t)
+    kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
+    plan = lib.StepPlan(stage.d["q"], stage.d["k_new"], stage.d["v_new"], stage.d["slot_mapping"],
+                        kc, vc, stage.d["block_tables"], stage.d["context_lens"], w.scale,
+                        int(w.context_lens.max()))
+    out_h = torch.empty(plan.out.shape, dtype=plan.out.dtype).pin_memory()
+    plan.capture_graph(before=stage.upload, after=lambda: out_h.copy_(plan.out, non_blocking=True))
+    for rep in range(2):
+        stage.h["q"].copy_(src["q"] * (1.0 + rep))
+        plan.replay()
+        torch.cuda.synchronize(dev)
+        got = out_h.clone()
+        assert torch.equal(stage.d["q"].cpu(), stage.h["q"])      # the replay uploaded
+        plan()                                   # the same step outside the graph
+        torch.cuda.synchronize(dev)
+        assert torch.equal(got, plan.out.cpu())
+        ref = lib.decode(stage.d["q"], kc, vc, stage.d["block_tables"], stage.d["context_lens"],
+                         w.scale)
+        torch.cuda.synchronize(dev)
+        assert torch.allclose(got.float(), ref.float().cpu(), atol=2e-3, rtol=1e-2)
+    assert lib.read_device_errors(dev) == 0
+
+
+def test_copy_async_between_pinned_host_and_device(dev):
+    """pa_copy_async moves bytes exactly between pinned host and device memory
+    in both directions and within the device; bad sizes are refused."""
+    n = (1 << 20) + 4096 + 48                      # not a multiple of the grid's chunking
+    src = torch.randint(-2**31, 2**31 - 1, (n // 4,), dtype=torch.int32).pin_memory()
+    d1 = torch.empty(n // 4, dtype=torch.int32, device=dev)
+    d2 = torch.empty_like(d1)
+    back = torch.empty(n // 4, dtype=torch.int32).pin_memory()
+    lib.copy_async(d1, src)
+    lib.copy_async(d2, d1)
+    lib.copy_async(back, d2)
+    torch.cuda.synchronize(dev)
+    assert torch.equal(back, src)
+    with pytest.raises(lib.PaError):
+        lib.copy_async(d1[1:5], src[1:5])          # 4-byte aligned, not 16
+    with pytest.raises(ValueError):
+        lib.copy_async(d1, torch.empty(n // 4, dtype=torch.int32))   # pageable host memory
