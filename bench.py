@@ -49,7 +49,7 @@ KERNEL_SOURCES = {
     "paged_decode_split": ["decode_kernel.cuh"] + _TILE_SOURCES,
     "paged_decode_step": ["decode_kernel.cuh"] + _TILE_SOURCES,
     "balanced_step": ["balanced.cu"] + _TILE_SOURCES,
-    "paged_prefill": ["prefill.cu"] + _TILE_SOURCES,
+    "paged_prefill": ["prefill.cu", "prefill_tc.cu", "tc_device.cuh"] + _TILE_SOURCES,
 }
 
 
@@ -654,7 +654,7 @@ def bench_prefill(args):
                        "l2": "flushed before every call (outside its events)"},
             "roofline": {"bound": "tensor", "kernel": "paged_prefill", "achieved": round(tflops / world, 2),
                          "peak": peak, "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, "
-                                                      "burst; mma.sync m16n8k16 path)",
+                                                      "burst; tcgen05 kernel, kernel='auto')",
                          "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4),
                          "traffic": None},
             "clocks": clk, "gpu_launches": args.steps,

@@ -22,10 +22,10 @@
 //   O  += P_j V_j          128 x 128 x 128, P read from tensor memory, V from
 //                          its TMA-staged [key][dim] tile (MN-major), O in
 //                          tensor memory
-// Warp roles: warp 0 streams K (three stages) and V (two stages) tiles with
-// TMA, 16-token boxes of the paged cache, K two tiles ahead of V; lane 0 of
-// warp 1 issues every MMA and commits it to mbarriers; warps 2-17 run the
-// softmax and the epilogue.  S_{j+1} is issued before P_j is ready, and P_j
+// Warp roles: warp 0 streams K tiles (two stages) and warp 18 V tiles (three
+// stages) with TMA, 16-token boxes of the paged cache, each at its own pace;
+// lane 0 of warp 1 issues every MMA and commits it to mbarriers; warps 2-17
+// run the softmax and the epilogue.  S_{j+1} is issued before P_j is ready, and P_j
 // is computed before P_{j-1} V_{j-1} has finished, so only the store of P
 // waits on the previous product.  Every mbarrier wait gives up after 1 s and
 // flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
@@ -38,13 +38,14 @@ namespace pa {
 
 constexpr int kTcRows = 128;                 // query rows per CTA (tokens x heads)
 constexpr int kTcKeys = 128;                 // keys per K/V tile
-constexpr int kTcKStages = 3;                // K tiles in flight
-constexpr int kTcVStages = 2;                // V tiles in flight
+constexpr int kTcKStages = 2;                // K tiles in flight (free once S is computed)
+constexpr int kTcVStages = 3;                // V tiles in flight (held until P V is done)
 constexpr int kTcPerRow = 4;                 // softmax threads per query row
 constexpr int kTcRowKeys = 128 / kTcPerRow;   // keys (and output dims) of one thread
 constexpr int kTcSoftmaxWarps = 4 * kTcPerRow;
 
-constexpr int kTcThreads = (2 + kTcSoftmaxWarps) * 32;
+constexpr int kTcVWarp = 2 + kTcSoftmaxWarps;  // the V producer, after the softmax warps
+constexpr int kTcThreads = (3 + kTcSoftmaxWarps) * 32;
 constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0, S1, O, P
 constexpr int kTcOperand = 32768;            // 128 rows x 2 halves x 128 B
 constexpr int kTcHalf = 16384;               // one 64-element half: 128 rows x 128 B
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
-    if (warp >= 2) {
+    if (warp >= 2 && warp < kTcVWarp) {
         // Q rows as the K-major A operand: row r = (token r / G, head r % G);
         // rows past the chunk are zero; each of the row's threads loads a quarter
         const int r = (warp & 3) * 32 + lane, part = (warp - 2) >> 2;
@@ -149,17 +150,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
     const uint32_t tP = tmem + 384;                         // P: hi [384, 448), lo [448, 512)
 
-    if (warp == 0) {
+    if (warp == 0 || warp == kTcVWarp) {
         // ------------------------------------------------------------------
-        // producer: K and V tiles, 16-token boxes through the block table;
-        // boxes wholly past the context are not loaded.  K (three stages) runs
-        // two tiles ahead of V (two stages): K_j is free once S_j is computed,
-        // V_j only after P_j V_j: K_0, K_1, K_2, V_0, K_3, V_1, ...
+        // producers: K tiles (warp 0, two stages, free once S is computed) and
+        // V tiles (the last warp, three stages, held until P V is done), each
+        // 16-token boxes through the block table; boxes wholly past the
+        // context are not loaded
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            prefetch_tensor_map(&tmap_k);
-            prefetch_tensor_map(&tmap_v);
-        }
+        if (lane == 0) prefetch_tensor_map(warp == 0 ? &tmap_k : &tmap_v);
         const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
         // boxes of tile j: this lane's block id and token offset for box `lane`
         auto describe = [&](int j, int& nbox, int& blk, int& sub) {
@@ -201,11 +199,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return true;
         };
-        bool ok = load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, 0);
-        if (ok && n_tiles > 1) ok = load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, 1);
+        // warp 0 streams K, the last warp V, each at its own pace
+        bool ok = true;
         for (int j = 0; j < n_tiles && ok; ++j) {
-            if (j + 2 < n_tiles) ok = load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j + 2);
-            if (ok) ok = load(&tmap_v, v_full, v_empty, Lay::kV, kTcVStages, j);
+            ok = warp == 0 ? load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j)
+                           : load(&tmap_v, v_full, v_empty, Lay::kV, kTcVStages, j);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
