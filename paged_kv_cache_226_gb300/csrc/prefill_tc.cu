@@ -10,24 +10,26 @@
 //
 // Per 128-key tile j (keys 128 j .. 128 j + 127 through the block table):
 //   S_j = Q K_j^T          128 x 128 x 128 into tensor memory (two buffers),
-//                          Q and K from shared memory
+//                          Q from tensor memory (stored there once), K from
+//                          its TMA-staged tile in shared memory
 //   P_j = 2^(S_j - m)      sixteen softmax warps, four threads per row (32
 //                          keys each, row maxima and sums exchanged through
 //                          shared memory), a lazily raised running max m (log2
 //                          units, threshold 2^8: the accumulator is rescaled
 //                          in tensor memory only when a row's max grows by
-//                          more than that); P goes to tensor memory (bf16: a
-//                          hi and a lo part cut from the fp32 bits, together
-//                          exact to 2^-15)
+//                          more than that); P goes to tensor memory over S_j
+//                          (already in registers; bf16: a hi and a lo part
+//                          cut from the fp32 bits, together exact to 2^-15)
 //   O  += P_j V_j          128 x 128 x 128, P read from tensor memory, V from
 //                          its TMA-staged [key][dim] tile (MN-major), O in
 //                          tensor memory
-// Warp roles: warp 0 streams K tiles (two stages) and warp 18 V tiles (three
-// stages) with TMA, 16-token boxes of the paged cache, each at its own pace;
+// Warp roles: warp 0 streams K tiles and warp 18 V tiles (three stages each,
+// the shared memory Q no longer needs) with TMA, 16-token boxes of the paged cache, each at its own pace;
 // lane 0 of warp 1 issues every MMA and commits it to mbarriers; warps 2-17
 // run the softmax and the epilogue.  S_{j+1} is issued before P_j is ready, and P_j
 // is computed before P_{j-1} V_{j-1} has finished, so only the store of P
-// waits on the previous product.  Every mbarrier wait gives up after 1 s and
+// waits on the previous product.  The MMAs of one thread run in issue order,
+// so S_{j+2}, issued after P_j V_j, overwrites P_j only once it has been read.  Every mbarrier wait gives up after 1 s and
 // flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
 // iterations without waiting (so their barriers always complete), and tensor
 // memory is always released.
@@ -38,7 +40,7 @@ namespace pa {
 
 constexpr int kTcRows = 128;                 // query rows per CTA (tokens x heads)
 constexpr int kTcKeys = 128;                 // keys per K/V tile
-constexpr int kTcKStages = 2;                // K tiles in flight (free once S is computed)
+constexpr int kTcKStages = 3;                // K tiles in flight (free once S is computed)
 constexpr int kTcVStages = 3;                // V tiles in flight (held until P V is done)
 constexpr int kTcPerRow = 4;                 // softmax threads per query row
 constexpr int kTcRowKeys = 128 / kTcPerRow;   // keys (and output dims) of one thread
@@ -46,13 +48,12 @@ constexpr int kTcSoftmaxWarps = 4 * kTcPerRow;
 
 constexpr int kTcVWarp = 2 + kTcSoftmaxWarps;  // the V producer, after the softmax warps
 constexpr int kTcThreads = (3 + kTcSoftmaxWarps) * 32;
-constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0, S1, O, P
+constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0/P0, S1/P1, O, Q
 constexpr int kTcOperand = 32768;            // 128 rows x 2 halves x 128 B
 constexpr int kTcHalf = 16384;               // one 64-element half: 128 rows x 128 B
 
 struct TcLayout {
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTcOperand;
+    static constexpr int kK = 0;
     static constexpr int kV = kK + kTcKStages * kTcOperand;
     static constexpr int kBytes = kV + kTcVStages * kTcOperand;
     static constexpr int kDynamicSmem = kBytes + 1024;
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t k_full[kTcKStages], k_empty[kTcKStages];
     __shared__ __align__(8) uint64_t v_full[kTcVStages], v_empty[kTcVStages];
     __shared__ float xchg[3][kTcPerRow][kTcRows];   // row maxima (two sets by tile parity), sums
-    __shared__ __align__(8) uint64_t s_full[2], s_free[2], p_full, o_done;
+    __shared__ __align__(8) uint64_t s_full[2], q_full, p_full, o_done;
     __shared__ uint32_t tmem_base;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -109,6 +110,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int last_pos = L - C + t0 + rows - 1;             // the CTA's last query position
     const int n_tiles = last_pos / kTcKeys + 1;
 
+    // producers' loads: K or V of tile j, 16-token boxes through the block
+    // table; boxes wholly past the context are not loaded
+    const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
+    // boxes of tile j: this lane's block id and token offset for box `lane`
+    auto describe = [&](int j, int& nbox, int& blk, int& sub) {
+        const int key0 = j * kTcKeys;
+        nbox = min(8, (L - key0 + 15) / 16);
+        blk = 0, sub = 0;
+        if (lane < nbox) {
+            const int tok = key0 + 16 * lane;
+            blk = __ldg(table + tok / p.block_size);
+            sub = tok % p.block_size;
+        }
+    };
+    // one operand (K or V) of tile j into stage j % stages
+    auto load = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, int kind_off,
+                    int stages, int j) -> bool {
+        int nbox, blk, sub;
+        describe(j, nbox, blk, sub);
+        const int s = j % stages;
+        bool ok = true;
+        if (lane == 0) {
+            if (j >= stages && !mbar_wait(&empty[s], ((j / stages) - 1) & 1)) {
+                flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+                ok = false;
+            } else {
+                mbar_arrive_expect_tx(&full[s], (uint32_t)nbox * 2u * kBox16Bytes);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return false;
+        if (lane < nbox && (blk < 0 || blk >= p.num_blocks)) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+        uint8_t* dst = smem + kind_off + s * kTcOperand;
+        for (int i = 0; i < nbox; ++i) {
+            const int bi = __shfl_sync(0xffffffffu, blk, i);
+            const int si = __shfl_sync(0xffffffffu, sub, i);
+            if (lane == 0) {
+                tma_load_4d(dst + i * kBox16Bytes, map, &full[s], 0, g, si, bi);
+                tma_load_4d(dst + kTcHalf + i * kBox16Bytes, map, &full[s], kBoxElems, g, si, bi);
+            }
+        }
+        return true;
+    };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcKStages; ++s) {
             mbar_init(&k_full[s], 1);
@@ -118,90 +162,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], kTcSoftmaxWarps);         // one arrival per softmax warp
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
+        mbar_init(&q_full, kTcSoftmaxWarps);                // one arrival per softmax warp
         mbar_init(&p_full, kTcSoftmaxWarps);
         mbar_init(&o_done, 1);
         fence_barrier_init();
+        fence_proxy_async_smem();                           // the barriers, for the copy engine
+        prefetch_tensor_map(&tmap_k);
+    }
+    // the first K tiles go out at once (no stage to wait for), overlapping the
+    // Q load and the tensor-memory allocation
+    constexpr int kEarlyK = kTcKStages;
+    if (warp == 0) {
+        __syncwarp();
+        for (int j = 0; j < kEarlyK && j < n_tiles; ++j)
+            load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j);
     }
     if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
+    // Q row r = (token r / G, head r % G), rows past the chunk zero: each of
+    // the row's four softmax threads fetches a quarter (dims 32 part ..)
+    uint32_t qw[16];
     if (warp >= 2 && warp < kTcVWarp) {
-        // Q rows as the K-major A operand: row r = (token r / G, head r % G);
-        // rows past the chunk are zero; each of the row's threads loads a quarter
         const int r = (warp & 3) * 32 + lane, part = (warp - 2) >> 2;
         const int t = r / G, h = r % G;
-        uint8_t* dq = smem + Lay::kQ;
         const uint4* src = reinterpret_cast<const uint4*>(
             reinterpret_cast<const T*>(p.q) +
             ((size_t)(q0 + t0 + min(t, rows - 1)) * p.num_q_heads + (size_t)g * G + h) * 128);
 #pragma unroll
-        for (int c = 4 * part; c < 4 * part + 4; ++c) {
-            const uint4 v = t < rows ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(dq + tc_chunk(r, c)) = v;
+        for (int c = 0; c < 4; ++c) {
+            const uint4 v = t < rows ? __ldg(src + 4 * part + c) : make_uint4(0u, 0u, 0u, 0u);
+            qw[4 * c] = v.x, qw[4 * c + 1] = v.y, qw[4 * c + 2] = v.z, qw[4 * c + 3] = v.w;
         }
-        fence_proxy_async_smem();
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base;
     const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
-    const uint32_t tP = tmem + 384;                         // P: hi [384, 448), lo [448, 512)
+    const uint32_t tQ = tmem + 384;                         // Q: dims 2c, 2c+1 in column c
 
     if (warp == 0 || warp == kTcVWarp) {
         // ------------------------------------------------------------------
         // producers: K tiles (warp 0, two stages, free once S is computed) and
-        // V tiles (the last warp, three stages, held until P V is done), each
-        // 16-token boxes through the block table; boxes wholly past the
-        // context are not loaded
+        // V tiles (the last warp, three stages, held until P V is done)
         // ------------------------------------------------------------------
-        if (lane == 0) prefetch_tensor_map(warp == 0 ? &tmap_k : &tmap_v);
-        const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
-        // boxes of tile j: this lane's block id and token offset for box `lane`
-        auto describe = [&](int j, int& nbox, int& blk, int& sub) {
-            const int key0 = j * kTcKeys;
-            nbox = min(8, (L - key0 + 15) / 16);
-            blk = 0, sub = 0;
-            if (lane < nbox) {
-                const int tok = key0 + 16 * lane;
-                blk = __ldg(table + tok / p.block_size);
-                sub = tok % p.block_size;
-            }
-        };
-        // one operand (K or V) of tile j into stage j % stages
-        auto load = [&](const CUtensorMap* map, uint64_t* full, uint64_t* empty, int kind_off,
-                        int stages, int j) -> bool {
-            int nbox, blk, sub;
-            describe(j, nbox, blk, sub);
-            const int s = j % stages;
-            bool ok = true;
-            if (lane == 0) {
-                if (j >= stages && !mbar_wait(&empty[s], ((j / stages) - 1) & 1)) {
-                    flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
-                    ok = false;
-                } else {
-                    mbar_arrive_expect_tx(&full[s], (uint32_t)nbox * 2u * kBox16Bytes);
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) return false;
-            if (lane < nbox && (blk < 0 || blk >= p.num_blocks)) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
-            uint8_t* dst = smem + kind_off + s * kTcOperand;
-            for (int i = 0; i < nbox; ++i) {
-                const int bi = __shfl_sync(0xffffffffu, blk, i);
-                const int si = __shfl_sync(0xffffffffu, sub, i);
-                if (lane == 0) {
-                    tma_load_4d(dst + i * kBox16Bytes, map, &full[s], 0, g, si, bi);
-                    tma_load_4d(dst + kTcHalf + i * kBox16Bytes, map, &full[s], kBoxElems, g, si, bi);
-                }
-            }
-            return true;
-        };
+        if (lane == 0 && warp == kTcVWarp) prefetch_tensor_map(&tmap_v);
         // warp 0 streams K, the last warp V, each at its own pace
         bool ok = true;
-        for (int j = 0; j < n_tiles && ok; ++j) {
+        for (int j = warp == 0 ? kEarlyK : 0; j < n_tiles && ok; ++j) {
             ok = warp == 0 ? load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j)
                            : load(&tmap_v, v_full, v_empty, Lay::kV, kTcVStages, j);
         }
@@ -212,13 +220,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, kBf16, false);
             constexpr uint32_t kIdPV = idesc_f16(kTcRows, 128, kBf16, true);
-            const uint32_t aQ = smem_u32(smem + Lay::kQ);
-            bool ok = true;
+            bool ok = mbar_wait(&q_full, 0);
+            tc_fence_after_sync();
             for (int j = 0; j <= n_tiles && ok; ++j) {
                 if (j < n_tiles) {
                     const int s = j % kTcKStages, bb = j & 1;
+                    // S buffer bb last held P_{j-2}, read by the product issued
+                    // before this one
                     ok = mbar_wait(&k_full[s], (j / kTcKStages) & 1);
-                    if (ok && j >= 2) ok = mbar_wait(&s_free[bb], ((j - 2) >> 1) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t aK = smem_u32(smem + Lay::kK + s * kTcOperand);
@@ -226,8 +235,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-                        mma_f16_ss(dS, smem_desc_sw128(aQ + off, 16, 1024),
-                                   smem_desc_sw128(aK + off, 16, 1024), kIdS, kk > 0);
+                        mma_f16_ts(dS, tQ + 8 * kk, smem_desc_sw128(aK + off, 16, 1024), kIdS,
+                                   kk > 0);
                     }
                     mma_commit(&s_full[bb]);
                     mma_commit(&k_empty[s]);                // S_j has read K_j
@@ -239,6 +248,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t aV = smem_u32(smem + Lay::kV + s * kTcOperand);
+                    const uint32_t tP = (jp & 1) ? tS1 : tS0;    // P_{j-1} over S_{j-1}
 #pragma unroll
                     for (int part = 0; part < (kSplitP ? 2 : 1); ++part) {
 #pragma unroll
@@ -264,7 +274,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int pos = min(L - C + t0 + t, L - 1);
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t my_cols = lane_addr + kTcRowKeys * part;
+        const float sl = p.scale_log2;
         float m = -INFINITY, l = 0.f;
+        // this thread's quarter of its Q row into tensor memory: 16 columns
+        tmem_st16(tQ + lane_addr + 16 * part, qw);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full);
         bool failed = false;                 // a wait ran out: finish the loop without waiting
         auto wait = [&](uint64_t* bar, uint32_t parity) {
             if (!failed && !__all_sync(0xffffffffu, mbar_wait(bar, parity))) failed = true;
@@ -272,7 +289,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the four threads' values of this row, through shared set `set`
         auto exchange = [&](int set, float v) {
             xchg[set][part][r] = v;
-            asm volatile("bar.sync 1, %0;" ::"n"(kTcSoftmaxWarps * 32) : "memory");
+            // the row's four threads sit in the four softmax warps of lane
+            // quarter warp % 4: one named barrier (1 + warp % 4) per quarter
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + (warp & 3)), "n"(kTcPerRow * 32) : "memory");
             return make_float4(xchg[set][0][r], xchg[set][1][r], xchg[set][2][r], xchg[set][3][r]);
         };
         for (int j = 0; j < n_tiles; ++j) {
@@ -287,26 +306,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(v0[k]);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[bb]);
-            // causal mask (only on tiles that reach past this row's position),
-            // log2 units, the row max over the four threads (eight independent
-            // partial maxima and sums keep the dependency chains short)
+            // causal mask (only on tiles that reach past this row's position)
+            // and the row max over the four threads, on the raw scores (the
+            // scale is positive; eight independent partial maxima and sums
+            // keep the dependency chains short)
             const int key0 = j * kTcKeys + kTcRowKeys * part;
             float pm[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) pm[i] = -INFINITY;
+            for (int e = 0; e < 8; ++e) pm[e] = -INFINITY;
             if (key0 + kTcRowKeys - 1 <= pos) {
 #pragma unroll
-                for (int k = 0; k < kTcRowKeys; ++k) {
-                    x[k] *= p.scale_log2;
-                    pm[k & 7] = fmaxf(pm[k & 7], x[k]);
-                }
+                for (int k = 0; k < kTcRowKeys; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < kTcRowKeys; ++k) {
-                    x[k] = key0 + k <= pos ? x[k] * p.scale_log2 : -INFINITY;
+                    x[k] = key0 + k <= pos ? x[k] : -INFINITY;
                     pm[k & 7] = fmaxf(pm[k & 7], x[k]);
                 }
             }
@@ -316,20 +330,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // two column sets by tile parity: a set is rewritten only after
                 // every thread has passed the next tile's barrier
                 const float4 e4 = exchange(bb, mx);
-                mx = fmaxf(fmaxf(e4.x, e4.y), fmaxf(e4.z, e4.w));
+                mx = fmaxf(fmaxf(e4.x, e4.y), fmaxf(e4.z, e4.w)) * sl;   // log2 units
             }
             // the reference max: raised only when the row max grows past 2^8
             const bool need = j > 0 && mx > m + kRescaleThresholdLog2;
             const float f = need ? ex2(m - mx) : 1.f;
             if (j == 0 || need) m = mx;                     // key 0 is visible to every row
-            // P = 2^(x - m) in registers (before the previous product has finished)
+            // P = 2^(x scale log2(e) - m) in registers (before the previous
+            // product has finished)
             uint32_t hi[kTcRowKeys / 2], lo[kTcRowKeys / 2];
             float ps[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ps[i] = 0.f;
+            for (int e = 0; e < 8; ++e) ps[e] = 0.f;
 #pragma unroll
             for (int e = 0; e < kTcRowKeys / 2; ++e) {
-                const float p0 = ex2(x[2 * e] - m), p1 = ex2(x[2 * e + 1] - m);
+                const float p0 = ex2(fmaf(x[2 * e], sl, -m)), p1 = ex2(fmaf(x[2 * e + 1], sl, -m));
                 if (kSplitP) {
                     // bf16 hi = p with its low 16 bits cut off (exact in fp32), lo =
                     // the remainder, also cut to bf16: hi + lo carries p to 2^-15,
@@ -371,9 +386,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         *reinterpret_cast<uint4*>(vd + tc_chunk(r, c)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // P into tensor memory as the A operand of P V: keys 2c, 2c+1 in
-            // column c of [384, 448) (bf16: lo parts in [448, 512)); this
+            // P into tensor memory over S_j, the A operand of P V: keys 2c,
+            // 2c+1 in column c of [0, 64) (bf16: lo parts in [64, 128)); this
             // thread's 32 keys are 16 columns at 16 part
+            const uint32_t tP = bb ? tS1 : tS0;
             tmem_st16(tP + lane_addr + 16 * part, hi);
             if (kSplitP) tmem_st16(tP + lane_addr + 64 + 16 * part, lo);
             tmem_wait_st();
