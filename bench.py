@@ -607,9 +607,14 @@ def bench_prefill(args):
     out = torch.empty_like(d["q"])
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
+    shp = lib.make_shape(w.num_seqs, d["q"].shape[1], d["kc"], d["bt"].shape[1])
+    ws_bytes = lib.prefill_workspace_size(shp, max_q)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    launches_per_call = 2 if ws_bytes else 1          # the ordering plan, then attention
 
     def call():
-        lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q, out)
+        lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q, out,
+                    workspace=ws)
 
     for _ in range(args.warmup):
         flush(1.0)
@@ -657,7 +662,7 @@ def bench_prefill(args):
                                                       "burst; tcgen05 kernel, kernel='auto')",
                          "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4),
                          "traffic": None},
-            "clocks": clk, "gpu_launches": args.steps,
+            "clocks": clk, "gpu_launches": args.steps * launches_per_call,
             "device_errors": lib.read_device_errors(dev)}
     if rank == 0:
         print(json.dumps(line), flush=True)

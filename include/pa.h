@@ -248,6 +248,30 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
                const pa_shape* shp, void* stream);
 
 /*
+ * pa_prefill_ws: pa_prefill with a workspace in which a one-CTA plan kernel
+ * orders the tcgen05 kernel's (sequence, chunk) work items by the number of
+ * key tiles they read, longest first, so that the longest start first and
+ * the SMs finish together (pa_prefill, without one, takes each sequence's
+ * chunks last-first: later chunks read more keys).  The pages describe
+ * prefill cost growing with the square of the prompt length (ta-paperlens
+ * page, the quadratic cost of prefill); the ordering itself is this
+ * library's.  workspace: device memory of at least
+ * pa_prefill_workspace_size(shp, max_query_len) bytes, 16-byte aligned, no
+ * initial contents, owned by the caller; calls that overlap on the GPU must
+ * not share it.  A size of 0 (the mma.sync kernel is taken) accepts a null
+ * workspace, which otherwise also falls back to pa_prefill's order.  Too
+ * small or misaligned: PA_ERR_INVALID_ARG.  Two launches when the tcgen05
+ * kernel is taken with a workspace, else one.  Results are bitwise the same
+ * as pa_prefill's.
+ */
+size_t pa_prefill_workspace_size(const pa_shape* shp, int32_t max_query_len);
+int pa_prefill_ws(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens,
+                  const int32_t* query_start, float scale, int32_t max_query_len,
+                  void* workspace, size_t workspace_bytes, void* out, const pa_shape* shp,
+                  void* stream);
+
+/*
  * pa_prefill_mma: the same operation, arguments and errors as pa_prefill,
  * always on the mma.sync kernel (16 query tokens per CTA, any group size and
  * head_dim 64 or 128).  pa_prefill takes the tcgen05 kernel (128 query rows

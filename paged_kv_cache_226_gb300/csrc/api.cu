@@ -434,10 +434,24 @@ int decode_step_balanced(const void* q, const void* k, const void* v, const int6
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+// Whether pa_prefill takes the tcgen05 kernel: head_dim 128, a group of 1, 2,
+// 4 or 8, a positive scale, and chunks that can fill its 128 rows.
+bool prefill_uses_tc(const pa_shape* shp, float scale, int32_t max_query_len) {
+    const int group = shp->num_q_heads / shp->num_kv_heads;
+    return pa::prefill_tc_supported(shp->head_dim, group, scale) && max_query_len >= 128 / group;
+}
+
+size_t prefill_sched_bytes(const pa_shape* shp, int32_t max_query_len) {
+    const int group = shp->num_q_heads / shp->num_kv_heads;
+    const size_t n = (size_t)shp->num_seqs * pa::prefill_tc_chunks(group, max_query_len);
+    return (n * sizeof(int32_t) + 255) & ~(size_t)255;
+}
+
 int prefill_any(const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* block_tables, const int32_t* context_lens,
-                const int32_t* query_start, float scale, int32_t max_query_len, void* out,
-                const pa_shape* shp, void* stream, bool mma_sync_only) {
+                const int32_t* query_start, float scale, int32_t max_query_len, void* workspace,
+                size_t workspace_bytes, void* out, const pa_shape* shp, void* stream,
+                bool mma_sync_only) {
     int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
     if (st != PA_OK) return st;
     if (max_query_len < 0) return PA_ERR_INVALID_ARG;
@@ -466,10 +480,20 @@ int prefill_any(const void* q, const void* k_cache, const void* v_cache,
     p.block_size = shp->block_size;
     p.num_blocks = shp->num_blocks;
     // the tcgen05 kernel's 128-row tiles pay off once a chunk can fill one
-    if (pa::prefill_tc_supported(shp->head_dim, p.group, scale) && !mma_sync_only &&
-        max_query_len >= 128 / p.group) {
-        e = pa::launch_prefill_tc(shp->dtype, tmk, tmv, p, max_query_len, shp->num_kv_heads,
-                                  shp->num_seqs, static_cast<cudaStream_t>(stream));
+    if (!mma_sync_only && prefill_uses_tc(shp, scale, max_query_len)) {
+        p.max_chunks = pa::prefill_tc_chunks(p.group, max_query_len);
+        p.num_seqs = shp->num_seqs;
+        if ((int64_t)p.num_seqs * p.max_chunks * shp->num_kv_heads > 0x7fffffffll)
+            return PA_ERR_UNSUPPORTED;
+        const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+        if (workspace) {
+            if (!aligned16(workspace) || workspace_bytes < prefill_sched_bytes(shp, max_query_len))
+                return PA_ERR_INVALID_ARG;
+            int32_t* sched = static_cast<int32_t*>(workspace);
+            e = pa::launch_prefill_tc_plan(p, sched, st_);
+            p.sched = sched;
+        }
+        if (e == cudaSuccess) e = pa::launch_prefill_tc(shp->dtype, tmk, tmv, p, shp->num_kv_heads, st_);
     } else {
         dim3 grid((unsigned)qtiles, shp->num_kv_heads, shp->num_seqs);
         e = pa::launch_prefill(shp->dtype, shp->head_dim, tmk, tmv, p, grid,
@@ -602,7 +626,24 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
                const int32_t* query_start, float scale, int32_t max_query_len, void* out,
                const pa_shape* shp, void* stream) {
     return prefill_any(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
-                       max_query_len, out, shp, stream, false);
+                       max_query_len, nullptr, 0, out, shp, stream, false);
+}
+
+size_t pa_prefill_workspace_size(const pa_shape* shp, int32_t max_query_len) {
+    if (!shp || shp->num_seqs <= 0 || shp->num_kv_heads <= 0 || max_query_len <= 0 ||
+        shp->num_q_heads % shp->num_kv_heads != 0)
+        return 0;
+    // the ordering is only used by the tcgen05 kernel; its scale test is on sign
+    return prefill_uses_tc(shp, 1.f, max_query_len) ? prefill_sched_bytes(shp, max_query_len) : 0;
+}
+
+int pa_prefill_ws(const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens,
+                  const int32_t* query_start, float scale, int32_t max_query_len,
+                  void* workspace, size_t workspace_bytes, void* out, const pa_shape* shp,
+                  void* stream) {
+    return prefill_any(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                       max_query_len, workspace, workspace_bytes, out, shp, stream, false);
 }
 
 int pa_prefill_mma(const void* q, const void* k_cache, const void* v_cache,
@@ -610,7 +651,7 @@ int pa_prefill_mma(const void* q, const void* k_cache, const void* v_cache,
                    const int32_t* query_start, float scale, int32_t max_query_len, void* out,
                    const pa_shape* shp, void* stream) {
     return prefill_any(q, k_cache, v_cache, block_tables, context_lens, query_start, scale,
-                       max_query_len, out, shp, stream, true);
+                       max_query_len, nullptr, 0, out, shp, stream, true);
 }
 
 int pa_copy_async(void* dst, const void* src, size_t nbytes, void* stream) {

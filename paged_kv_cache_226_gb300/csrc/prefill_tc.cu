@@ -85,13 +85,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int qt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group;
     const int QT = kTcRows / G;                             // new tokens per CTA
+    const int num_kv_heads = p.num_q_heads / G;
 
     grid_dependency_wait();
     allow_dependent_launch();
+    // CTAs start in index order: rank r takes the r-th (sequence, chunk) item
+    // of the schedule, for every KV head in turn
+    const int g = (int)(blockIdx.x % (unsigned)num_kv_heads);
+    const int rank = (int)(blockIdx.x / (unsigned)num_kv_heads);
+    const int n_items = p.num_seqs * p.max_chunks;
+    const int item = p.sched ? p.sched[rank] : n_items - 1 - rank;
+    if (item < 0) return;
+    const int b = item / p.max_chunks, qt = item % p.max_chunks;
     const int max_ctx = p.max_blocks_per_seq * p.block_size;
     int L = p.context_lens[b];
     if (L < 0 || L > max_ctx) {
@@ -450,11 +458,85 @@ bool prefill_tc_supported(int head_dim, int group, float scale) {
     return head_dim == 128 && (group == 1 || group == 2 || group == 4 || group == 8) && scale > 0.f;
 }
 
+int prefill_tc_chunks(int group, int max_query_len) {
+    const int qt = kTcRows / group;
+    return (max_query_len + qt - 1) / qt;
+}
+
+// Counting sort of the items by key-tile count, descending; the order inside
+// one count is whatever the atomics give (every item is computed alone, so
+// the results do not depend on it).
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 4096;               // counts above 4095 share the top bucket
+
+__device__ __forceinline__ int prefill_item_tiles(const PrefillParams& p, int item) {
+    const int b = item / p.max_chunks, qt = item % p.max_chunks, QT = kTcRows / p.group;
+    const int max_ctx = p.max_blocks_per_seq * p.block_size;
+    const int L = min(max(p.context_lens[b], 0), max_ctx);
+    const int C = min(p.query_start[b + 1] - p.query_start[b], L);
+    const int t0 = qt * QT;
+    if (t0 >= C) return 0;
+    return min((L - C + t0 + min(QT, C - t0) - 1) / kTcKeys + 1, kPlanBuckets - 1);
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+    prefill_tc_plan_kernel(const __grid_constant__ PrefillParams p, int32_t* sched) {
+    __shared__ int offs[kPlanBuckets];
+    __shared__ int warp_sum[kPlanThreads / 32];
+    grid_dependency_wait();
+    allow_dependent_launch();
+    const int n = p.num_seqs * p.max_chunks, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    for (int c = tid; c < kPlanBuckets; c += kPlanThreads) offs[c] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kPlanThreads) atomicAdd(&offs[prefill_item_tiles(p, i)], 1);
+    __syncthreads();
+    // exclusive scan in descending count order: thread tid owns the four
+    // buckets 4095 - 4 tid .. 4092 - 4 tid
+    constexpr int kPer = kPlanBuckets / kPlanThreads;
+    int own[kPer], sum = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        own[k] = offs[kPlanBuckets - 1 - (kPer * tid + k)];
+        sum += own[k];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) warp_sum[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int v = warp_sum[lane], vi = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, vi, d);
+            if (lane >= d) vi += u;
+        }
+        warp_sum[lane] = vi - v;                       // exclusive over warps
+    }
+    __syncthreads();
+    int run = warp_sum[w] + incl - sum;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        offs[kPlanBuckets - 1 - (kPer * tid + k)] = run;
+        run += own[k];
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += kPlanThreads) {
+        const int c = prefill_item_tiles(p, i);
+        sched[atomicAdd(&offs[c], 1)] = c > 0 ? i : -1;
+    }
+}
+
+cudaError_t launch_prefill_tc_plan(const PrefillParams& p, int32_t* sched, cudaStream_t stream) {
+    return launch_with_pdl(prefill_tc_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, p, sched);
+}
+
 cudaError_t launch_prefill_tc(int dtype, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                              const PrefillParams& p, int max_query_len, int num_kv_heads,
-                              int num_seqs, cudaStream_t stream) {
-    const int qt = kTcRows / p.group;
-    dim3 grid((unsigned)((max_query_len + qt - 1) / qt), num_kv_heads, num_seqs);
+                              const PrefillParams& p, int num_kv_heads, cudaStream_t stream) {
+    dim3 grid((unsigned)((int64_t)p.num_seqs * p.max_chunks * num_kv_heads));
     if (dtype == PA_BF16) return launch_prefill_tc_t<__nv_bfloat16>(tmk, tmv, p, grid, stream);
     return launch_prefill_tc_t<__half>(tmk, tmv, p, grid, stream);
 }

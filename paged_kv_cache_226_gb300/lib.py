@@ -87,6 +87,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         for fn in (lib.pa_prefill, lib.pa_prefill_mma):
             fn.argtypes = [V, V, V, V, V, V, F, I32, V, S, V]
             fn.restype = ctypes.c_int
+        lib.pa_prefill_workspace_size.argtypes = [S, I32]
+        lib.pa_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.pa_prefill_ws.argtypes = [V, V, V, V, V, V, F, I32, V, ctypes.c_size_t, V, S, V]
+        lib.pa_prefill_ws.restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [V, V, I64, V, V, I64, V, I64, S, V]
         lib.pa_copy_blocks.restype = ctypes.c_int
         lib.pa_decode_step.argtypes = [V, V, V, V, V, V, V, V, F, I32, I32, V, V, V, V, V, S, V]
@@ -525,10 +529,13 @@ def decode_step_balanced(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_
 
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
             max_query_len: int, out: Optional[torch.Tensor] = None,
-            kernel: str = "auto") -> torch.Tensor:
+            kernel: str = "auto", schedule: bool = True,
+            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Chunked-prefill attention (pa_prefill): the last C_b tokens of each
     sequence attend causally over its cache; q, out [total_tokens][Hq][D].
-    kernel "mma" forces the mma.sync kernel (pa_prefill_mma)."""
+    kernel "mma" forces the mma.sync kernel (pa_prefill_mma).  schedule: order
+    the tcgen05 kernel's work longest first (pa_prefill_ws, with ``workspace``
+    or a fresh one of pa_prefill_workspace_size bytes); False: pa_prefill."""
     lib = load()
     dev = k_cache.device
     _need(q, "q", k_cache.dtype, dev)
@@ -543,12 +550,23 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale:
     out = torch.empty_like(q) if out is None else out
     _need(out, "out", q.dtype, dev)
     shp = make_shape(B, q.shape[1], k_cache, block_tables.shape[1])
-    fn = lib.pa_prefill_mma if kernel == "mma" else lib.pa_prefill
-    _check("pa_prefill", fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                        _ptr(context_lens), _ptr(query_start), float(scale),
-                                        int(max_query_len), _ptr(out), ctypes.byref(shp),
-                                        _stream_handle(dev)))
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+            _ptr(query_start), float(scale), int(max_query_len))
+    if kernel == "mma" or not schedule:
+        fn = lib.pa_prefill_mma if kernel == "mma" else lib.pa_prefill
+        _check("pa_prefill", fn(*args, _ptr(out), ctypes.byref(shp), _stream_handle(dev)))
+        return out
+    if workspace is None:
+        n = prefill_workspace_size(shp, max_query_len)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    _check("pa_prefill_ws", lib.pa_prefill_ws(*args, _ptr(workspace), workspace.numel(), _ptr(out),
+                                              ctypes.byref(shp), _stream_handle(dev)))
     return out
+
+
+def prefill_workspace_size(shp, max_query_len: int) -> int:
+    """Bytes of the work-ordering workspace pa_prefill_ws needs (0: none)."""
+    return int(load().pa_prefill_workspace_size(ctypes.byref(shp), int(max_query_len)))
 
 
 STATIC_WORKSPACE_BYTES = 32 << 20

@@ -2,7 +2,9 @@
 the chunk's K/V written with pa_reshape_and_cache, then causal attention of
 every new token against the fp64 reference, |gpu - ref| <= 2e-3 + 1e-2 |ref|.
 Both kernels are checked: the tcgen05 one (head_dim 128, groups 1/2/4/8,
-what pa_prefill takes there) and the mma.sync one (pa_prefill_mma)."""
+what pa_prefill takes there), with its work ordered longest first
+(pa_prefill_ws, "auto") or last chunk first (pa_prefill, "unscheduled"), and
+the mma.sync one (pa_prefill_mma)."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +28,14 @@ def dev():
     return d
 
 
+def _run(d, w, max_q, kernel):
+    if kernel == "unscheduled":
+        return lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q,
+                           schedule=False)
+    return lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q,
+                       kernel=kernel)
+
+
 def _check_prefill(w, dev, kernel="auto"):
     d = {k: (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).to(dev)
          for k, v in dict(q=w.q, kn=w.k_new, vn=w.v_new, kc=w.k_cache, vc=w.v_cache,
@@ -33,8 +43,7 @@ def _check_prefill(w, dev, kernel="auto"):
                           sm=w.slot_mapping).items()}
     lib.reshape_and_cache(d["kn"], d["vn"], d["sm"], d["kc"], d["vc"])
     max_q = int(np.diff(w.query_start).max()) if w.num_seqs else 0
-    out = lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q,
-                      kernel=kernel)
+    out = _run(d, w, max_q, kernel)
     kc, vc, _ = oracle.reshape_and_cache(pin.bits(w.k_new), pin.bits(w.v_new), w.slot_mapping,
                                          pin.bits(w.k_cache), pin.bits(w.v_cache), w.block_size)
     want = oracle.paged_prefill(pin.bits(w.q), kc, vc, w.block_tables, w.context_lens,
@@ -46,7 +55,7 @@ def _check_prefill(w, dev, kernel="auto"):
     return err
 
 
-@pytest.mark.parametrize("kernel", ["auto", "mma"])
+@pytest.mark.parametrize("kernel", ["auto", "unscheduled", "mma"])
 @pytest.mark.parametrize("name", ["prefill_tiny", "prefill8b"])
 def test_named_prefill(dev, name, kernel):
     _check_prefill(pin.build_prefill_workload(name), dev, kernel)
@@ -56,14 +65,14 @@ def test_named_prefill(dev, name, kernel):
     ("fp16", 8, 2, 64, 16), ("bf16", 32, 8, 128, 16), ("fp16", 64, 8, 128, 32),
     ("bf16", 4, 4, 128, 16), ("fp16", 16, 8, 64, 32), ("bf16", 12, 2, 128, 16),
     ("fp16", 16, 8, 128, 16)])
-@pytest.mark.parametrize("kernel", ["auto", "mma"])
+@pytest.mark.parametrize("kernel", ["auto", "unscheduled", "mma"])
 def test_prefill_shapes_and_ragged_chunks(dev, dtype, hq, hkv, d, bs, kernel):
     lens = [1, 15, 16, 17, 33, 100, 257, 700, 40]
     chunks = [1, 15, 1, 17, 16, 37, 257, 300, 0]
     w = pin.build_prefill_workload(params=dict(dtype=dtype, lens=lens, chunks=chunks,
                                                num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                                                block_size=bs), seed=hq + d + bs)
-    _check_prefill(w, dev)
+    _check_prefill(w, dev, kernel)
 
 
 def test_one_token_chunks_equal_decode(dev):
@@ -119,3 +128,44 @@ def test_prefill_stale_nan_outside_the_contexts(dev, dtype, bs, kernel):
     w.k_cache = torch.from_numpy(kc.view(np.int16)).view(tdt)
     w.v_cache = torch.from_numpy(vc.view(np.int16)).view(tdt)
     _check_prefill(w, dev, kernel)
+
+
+def test_prefill_work_order_is_bitwise_irrelevant(dev):
+    """Each (sequence, chunk, KV head) is computed by one CTA alone: the
+    longest-first order and the last-chunk-first order give the same bits.
+    The ragged batch has chunks of 1 to 900 tokens on contexts of 1 to 4100."""
+    w = pin.build_prefill_workload(params=dict(dtype="bf16", lens=[4100, 1, 900, 2000, 77, 3000],
+                                               chunks=[300, 1, 900, 33, 77, 1],
+                                               num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                               block_size=16), seed=61)
+    d = {k: (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).to(dev)
+         for k, v in dict(q=w.q, kc=w.k_cache, vc=w.v_cache, bt=w.block_tables,
+                          cl=w.context_lens, qs=w.query_start).items()}
+    max_q = int(np.diff(w.query_start).max())
+    a = _run(d, w, max_q, "auto")
+    b = _run(d, w, max_q, "unscheduled")
+    torch.cuda.synchronize(dev)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert lib.read_device_errors(dev) == 0
+
+
+def test_prefill_workspace_size_and_errors(dev):
+    w = pin.build_prefill_workload("prefill8b")
+    d = {k: (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).to(dev)
+         for k, v in dict(q=w.q, kc=w.k_cache, vc=w.v_cache, bt=w.block_tables,
+                          cl=w.context_lens, qs=w.query_start).items()}
+    max_q = int(np.diff(w.query_start).max())
+    shp = lib.make_shape(w.num_seqs, d["q"].shape[1], d["kc"], d["bt"].shape[1])
+    n = lib.prefill_workspace_size(shp, max_q)
+    # 512-token chunks, 32 tokens (x 4 heads) per CTA: 16 chunks per sequence
+    assert n == 256 * -(-4 * w.num_seqs * 16 // 256)
+    small = torch.empty(16, dtype=torch.uint8, device=dev)
+    with pytest.raises(lib.PaError, match="invalid"):
+        lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q,
+                    workspace=small)
+    # head_dim 64 takes the mma.sync kernel: no workspace needed
+    q64 = torch.zeros((4, 8, 64), dtype=torch.float16, device=dev)
+    kc64 = torch.zeros((4, 16, 2, 64), dtype=torch.float16, device=dev)
+    bt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    assert lib.prefill_workspace_size(lib.make_shape(1, 8, kc64, 1), 4) == 0
+    assert lib.read_device_errors(dev) == 0
