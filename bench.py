@@ -49,7 +49,7 @@ KERNEL_SOURCES = {
     "paged_decode_split": ["decode_kernel.cuh"] + _TILE_SOURCES,
     "paged_decode_step": ["decode_kernel.cuh"] + _TILE_SOURCES,
     "balanced_step": ["balanced.cu"] + _TILE_SOURCES,
-    "paged_prefill": ["prefill.cu", "prefill_tc.cu", "tc_device.cuh"] + _TILE_SOURCES,
+    "paged_prefill": ["prefill.cu", "prefill_tc.cu", "tc_device.cuh", "prefill_internal.h"] + _TILE_SOURCES,
 }
 
 

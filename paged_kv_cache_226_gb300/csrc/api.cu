@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "pa_internal.h"
+#include "prefill_internal.h"
 
 namespace {
 

@@ -12,6 +12,7 @@
 // softmax per row, O += P V with P rounded to the 16-bit type (bf16: hi +
 // lo parts), P reused straight from the score fragments.
 #include "decode_tile.cuh"
+#include "prefill_internal.h"
 
 namespace pa {
 

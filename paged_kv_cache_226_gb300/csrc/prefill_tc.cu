@@ -34,6 +34,7 @@
 // iterations without waiting (so their barriers always complete), and tensor
 // memory is always released.
 #include "decode_tile.cuh"
+#include "prefill_internal.h"
 #include "tc_device.cuh"
 
 namespace pa {
