@@ -24,13 +24,14 @@
 //                          its TMA-staged [key][dim] tile (MN-major), O in
 //                          tensor memory
 // Warp roles: warp 0 streams K tiles and warp 18 V tiles (three stages each,
-// the shared memory Q no longer needs) with TMA, 16-token boxes of the paged cache, each at its own pace;
-// lane 0 of warp 1 issues every MMA and commits it to mbarriers; warps 2-17
-// run the softmax and the epilogue.  S_{j+1} is issued before P_j is ready, and P_j
-// is computed before P_{j-1} V_{j-1} has finished, so only the store of P
-// waits on the previous product.  The MMAs of one thread run in issue order,
-// so S_{j+2}, issued after P_j V_j, overwrites P_j only once it has been read.  Every mbarrier wait gives up after 1 s and
-// flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
+// in the shared memory Q does not need) with TMA, 16-token boxes of the paged
+// cache, each at its own pace; lane 0 of warp 1 issues every MMA and commits
+// it to mbarriers; warps 2-17 run the softmax and the epilogue.  S_{j+1} is
+// issued before P_j is ready, and P_j is computed before P_{j-1} V_{j-1} has
+// finished, so only the store of P waits on the previous product.  The MMAs
+// of one thread run in issue order, so S_{j+2}, issued after P_j V_j,
+// overwrites P_j only once it has been read.  Every mbarrier wait gives up
+// after 1 s and flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
 // iterations without waiting (so their barriers always complete), and tensor
 // memory is always released.
 #include "decode_tile.cuh"
@@ -176,16 +177,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(&p_full, kTcSoftmaxWarps);
         mbar_init(&o_done, 1);
         fence_barrier_init();
-        fence_proxy_async_smem();                           // the barriers, for the copy engine
-        prefetch_tensor_map(&tmap_k);
-    }
-    // the first K tiles go out at once (no stage to wait for), overlapping the
-    // Q load and the tensor-memory allocation
-    constexpr int kEarlyK = kTcKStages;
-    if (warp == 0) {
-        __syncwarp();
-        for (int j = 0; j < kEarlyK && j < n_tiles; ++j)
-            load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j);
     }
     if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
     // Q row r = (token r / G, head r % G), rows past the chunk zero: each of
@@ -215,10 +206,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // producers: K tiles (warp 0, two stages, free once S is computed) and
         // V tiles (the last warp, three stages, held until P V is done)
         // ------------------------------------------------------------------
-        if (lane == 0 && warp == kTcVWarp) prefetch_tensor_map(&tmap_v);
-        // warp 0 streams K, the last warp V, each at its own pace
+        if (lane == 0) prefetch_tensor_map(warp == 0 ? &tmap_k : &tmap_v);
+        // warp 0 streams K, the last warp V, each at its own pace (issuing the
+        // first K tiles before the CTA barrier measured 7 % slower: their
+        // block-table reads hold the barrier up)
         bool ok = true;
-        for (int j = warp == 0 ? kEarlyK : 0; j < n_tiles && ok; ++j) {
+        for (int j = 0; j < n_tiles && ok; ++j) {
             ok = warp == 0 ? load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j)
                            : load(&tmap_v, v_full, v_empty, Lay::kV, kTcVStages, j);
         }
