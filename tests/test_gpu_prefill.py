@@ -169,3 +169,40 @@ def test_prefill_workspace_size_and_errors(dev):
     bt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
     assert lib.prefill_workspace_size(lib.make_shape(1, 8, kc64, 1), 4) == 0
     assert lib.read_device_errors(dev) == 0
+
+
+def test_prefill_work_order_is_a_longest_first_permutation(dev):
+    """The plan kernel's order (left in the workspace, int32 per item b * chunks
+    + chunk) holds every (sequence, chunk) item that has query tokens exactly
+    once, by non-increasing count of 128-key tiles, then -1 for the rest."""
+    lens = [4100, 1, 900, 2000, 77, 3000, 129, 640]
+    chunks = [300, 1, 900, 33, 77, 1, 129, 0]
+    w = pin.build_prefill_workload(params=dict(dtype="bf16", lens=lens, chunks=chunks,
+                                               num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                               block_size=16), seed=67)
+    d = {k: (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).to(dev)
+         for k, v in dict(q=w.q, kc=w.k_cache, vc=w.v_cache, bt=w.block_tables,
+                          cl=w.context_lens, qs=w.query_start).items()}
+    max_q = int(np.diff(w.query_start).max())
+    shp = lib.make_shape(w.num_seqs, 32, d["kc"], d["bt"].shape[1])
+    ws = torch.full((lib.prefill_workspace_size(shp, max_q),), 0x55, dtype=torch.uint8, device=dev)
+    lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q, workspace=ws)
+    torch.cuda.synchronize(dev)
+    qt = 128 // 4                                   # query tokens per item at G = 4
+    n_chunks = -(-max_q // qt)
+    n = w.num_seqs * n_chunks
+    order = ws.view(torch.int32)[:n].cpu().numpy()
+    tiles = {}
+    for b in range(w.num_seqs):
+        L, C = lens[b], chunks[b]
+        for c in range(n_chunks):
+            t0 = c * qt
+            if t0 < C:
+                rows = min(qt, C - t0)
+                tiles[b * n_chunks + c] = (L - C + t0 + rows - 1) // 128 + 1
+    valid = order[order >= 0]
+    assert sorted(valid.tolist()) == sorted(tiles)
+    assert (order[len(valid):] == -1).all()
+    counts = [tiles[i] for i in valid]
+    assert all(a >= b for a, b in zip(counts, counts[1:]))
+    assert lib.read_device_errors(dev) == 0
