@@ -25,13 +25,15 @@
 //                          tensor memory
 // Warp roles: warp 0 streams K tiles and warp 18 V tiles (three stages each,
 // in the shared memory Q does not need) with TMA, 16-token boxes of the paged
-// cache, each at its own pace; lane 0 of warp 1 issues every MMA and commits
-// it to mbarriers; warps 2-17 run the softmax and the epilogue.  S_{j+1} is
-// issued before P_j is ready, and P_j is computed before P_{j-1} V_{j-1} has
-// finished, so only the store of P waits on the previous product.  The MMAs
-// of one thread run in issue order, so S_{j+2}, issued after P_j V_j,
-// overwrites P_j only once it has been read.  Every mbarrier wait gives up
-// after 1 s and flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
+// cache, each at its own pace; lane 0 of warp 1 issues the S products and
+// lane 0 of warp 19 the P V products, committing them to mbarriers; warps
+// 2-17 run the softmax and the epilogue.  One control warp sits on each of
+// the SM's four schedulers: a thread issuing MMAs beside warps with ALU work
+// ready is starved of issue slots, and two issuers halve what each must get
+// through.  S_{j+1} is issued before P_j is ready, and P_j is computed before
+// P_{j-1} V_{j-1} has finished, so only the store of P waits on the previous
+// product; S_{j+2} overwrites P_j, so its issuer waits for P_j V_j first.
+// Every mbarrier wait gives up after 1 s and flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
 // iterations without waiting (so their barriers always complete), and tensor
 // memory is always released.
 #include "decode_tile.cuh"
@@ -49,7 +51,8 @@ constexpr int kTcRowKeys = 128 / kTcPerRow;   // keys (and output dims) of one t
 constexpr int kTcSoftmaxWarps = 4 * kTcPerRow;
 
 constexpr int kTcVWarp = 2 + kTcSoftmaxWarps;  // the V producer, after the softmax warps
-constexpr int kTcThreads = (3 + kTcSoftmaxWarps) * 32;
+constexpr int kTcPvWarp = 3 + kTcSoftmaxWarps; // issues P V (warp 1 issues S)
+constexpr int kTcThreads = (4 + kTcSoftmaxWarps) * 32;
 constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0/P0, S1/P1, O, Q
 constexpr int kTcOperand = 32768;            // 128 rows x 2 halves x 128 B
 constexpr int kTcHalf = 16384;               // one 64-element half: 128 rows x 128 B
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t k_full[kTcKStages], k_empty[kTcKStages];
     __shared__ __align__(8) uint64_t v_full[kTcVStages], v_empty[kTcVStages];
     __shared__ float xchg[3][kTcPerRow][kTcRows];   // row maxima (two sets by tile parity), sums
-    __shared__ __align__(8) uint64_t s_full[2], q_full, p_full, o_done;
+    __shared__ __align__(8) uint64_t s_full[2], q_full, p_full, o_done[2];
     __shared__ uint32_t tmem_base;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
         mbar_init(&q_full, kTcSoftmaxWarps);                // one arrival per softmax warp
         mbar_init(&p_full, kTcSoftmaxWarps);
-        mbar_init(&o_done, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&o_done[i], 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
@@ -215,21 +218,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = warp == 0 ? load(&tmap_k, k_full, k_empty, Lay::kK, kTcKStages, j)
                            : load(&tmap_v, v_full, v_empty, Lay::kV, kTcVStages, j);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kTcPvWarp) {
         // ------------------------------------------------------------------
-        // MMA issuer: S_j, then P_{j-1} V_{j-1}
+        // MMA issuers, one thread each on two schedulers: warp 1 issues S_j,
+        // the last warp P_j V_j.  S_j overwrites P_{j-2}, so it waits for that
+        // product (o_done by tile parity); P V in order accumulates O.
         // ------------------------------------------------------------------
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, kBf16, false);
             constexpr uint32_t kIdPV = idesc_f16(kTcRows, 128, kBf16, true);
-            bool ok = mbar_wait(&q_full, 0);
-            tc_fence_after_sync();
-            for (int j = 0; j <= n_tiles && ok; ++j) {
-                if (j < n_tiles) {
+            bool ok = true;
+            if (warp == 1) {
+                ok = mbar_wait(&q_full, 0);
+                tc_fence_after_sync();
+                for (int j = 0; j < n_tiles && ok; ++j) {
                     const int s = j % kTcKStages, bb = j & 1;
-                    // S buffer bb last held P_{j-2}, read by the product issued
-                    // before this one
                     ok = mbar_wait(&k_full[s], (j / kTcKStages) & 1);
+                    if (ok && j >= 2) ok = mbar_wait(&o_done[bb], ((j - 2) >> 1) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t aK = smem_u32(smem + Lay::kK + s * kTcOperand);
@@ -243,23 +248,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_commit(&s_full[bb]);
                     mma_commit(&k_empty[s]);                // S_j has read K_j
                 }
-                if (j >= 1) {
-                    const int jp = j - 1, s = jp % kTcVStages;
-                    ok = mbar_wait(&p_full, jp & 1);
-                    if (ok) ok = mbar_wait(&v_full[s], (jp / kTcVStages) & 1);
+            } else {
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    const int s = j % kTcVStages;
+                    ok = mbar_wait(&p_full, j & 1);
+                    if (ok) ok = mbar_wait(&v_full[s], (j / kTcVStages) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t aV = smem_u32(smem + Lay::kV + s * kTcOperand);
-                    const uint32_t tP = (jp & 1) ? tS1 : tS0;    // P_{j-1} over S_{j-1}
+                    const uint32_t tP = (j & 1) ? tS1 : tS0;    // P_j over S_j
 #pragma unroll
                     for (int part = 0; part < (kSplitP ? 2 : 1); ++part) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             mma_f16_ts(tO, tP + 64 * part + 8 * kk,
                                        smem_desc_sw128(aV + kk * 16 * 128, kTcHalf, 1024), kIdPV,
-                                       jp > 0 || part > 0 || kk > 0);
+                                       j > 0 || part > 0 || kk > 0);
                     }
-                    mma_commit(&o_done);
+                    mma_commit(&o_done[j & 1]);
                     mma_commit(&v_empty[s]);                // P_j V_j has read V_j
                 }
             }
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             l = l * f + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
             // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
             if (j > 0) {
-                wait(&o_done, (j - 1) & 1);
+                wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1);
                 tc_fence_after_sync();
             }
             if (__any_sync(0xffffffffu, need)) {
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive(&p_full);
         }
         // epilogue: O / l for the chunk's rows, l summed over the row's threads
-        wait(&o_done, (n_tiles - 1) & 1);
+        wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1);
         tc_fence_after_sync();
         const float4 l4 = exchange(2, l);
         if (!failed) {
