@@ -661,7 +661,7 @@ def bench_prefill(args):
                          "peak": peak, "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, "
                                                       "burst; tcgen05 kernel, kernel='auto')",
                          "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4),
-                         "traffic": None},
+                         "traffic": profiled_traffic(args.prefill_config, "paged_prefill")},
             "clocks": clk, "gpu_launches": args.steps * launches_per_call,
             "device_errors": lib.read_device_errors(dev)}
     if rank == 0:

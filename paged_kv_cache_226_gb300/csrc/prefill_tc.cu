@@ -33,9 +33,9 @@
 // through.  S_{j+1} is issued before P_j is ready, and P_j is computed before
 // P_{j-1} V_{j-1} has finished, so only the store of P waits on the previous
 // product; S_{j+2} overwrites P_j, so its issuer waits for P_j V_j first.
-// Every mbarrier wait gives up after 1 s and flags PA_DEVERR_WAIT_TIMEOUT; the softmax warps then run their remaining
-// iterations without waiting (so their barriers always complete), and tensor
-// memory is always released.
+// Every mbarrier wait gives up after 1 s and flags PA_DEVERR_WAIT_TIMEOUT;
+// the softmax warps then run their remaining iterations without waiting (so
+// their barriers always complete), and tensor memory is always released.
 #include "decode_tile.cuh"
 #include "prefill_internal.h"
 #include "tc_device.cuh"
@@ -206,11 +206,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0 || warp == kTcVWarp) {
         // ------------------------------------------------------------------
-        // producers: K tiles (warp 0, two stages, free once S is computed) and
-        // V tiles (the last warp, three stages, held until P V is done)
+        // producers: K tiles (warp 0, free once S is computed) and V tiles
+        // (warp 18, held until P V is done), three stages each
         // ------------------------------------------------------------------
         if (lane == 0) prefetch_tensor_map(warp == 0 ? &tmap_k : &tmap_v);
-        // warp 0 streams K, the last warp V, each at its own pace (issuing the
+        // warp 0 streams K, warp 18 V, each at its own pace (issuing the
         // first K tiles before the CTA barrier measured 7 % slower: their
         // block-table reads hold the barrier up)
         bool ok = true;
