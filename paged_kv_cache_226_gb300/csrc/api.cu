@@ -461,6 +461,10 @@ int prefill_any(const void* q, const void* k_cache, const void* v_cache,
         return PA_ERR_INVALID_ARG;
     const int64_t qtiles = (max_query_len + 15) / 16;
     if (qtiles > 0x7fffffffll) return PA_ERR_UNSUPPORTED;
+    const bool use_tc = !mma_sync_only && prefill_uses_tc(shp, scale, max_query_len);
+    if (use_tc && workspace &&
+        (!aligned16(workspace) || workspace_bytes < prefill_sched_bytes(shp, max_query_len)))
+        return PA_ERR_INVALID_ARG;
     CUtensorMap tmk, tmv;
     if ((st = encode_cache_map(&tmk, k_cache, shp, false)) != PA_OK) return st;
     if ((st = encode_cache_map(&tmv, v_cache, shp, false)) != PA_OK) return st;
@@ -481,15 +485,13 @@ int prefill_any(const void* q, const void* k_cache, const void* v_cache,
     p.block_size = shp->block_size;
     p.num_blocks = shp->num_blocks;
     // the tcgen05 kernel's 128-row tiles pay off once a chunk can fill one
-    if (!mma_sync_only && prefill_uses_tc(shp, scale, max_query_len)) {
+    if (use_tc) {
         p.max_chunks = pa::prefill_tc_chunks(p.group, max_query_len);
         p.num_seqs = shp->num_seqs;
         if ((int64_t)p.num_seqs * p.max_chunks * shp->num_kv_heads > 0x7fffffffll)
             return PA_ERR_UNSUPPORTED;
         const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
         if (workspace) {
-            if (!aligned16(workspace) || workspace_bytes < prefill_sched_bytes(shp, max_query_len))
-                return PA_ERR_INVALID_ARG;
             int32_t* sched = static_cast<int32_t*>(workspace);
             e = pa::launch_prefill_tc_plan(p, sched, st_);
             p.sched = sched;

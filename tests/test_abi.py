@@ -106,6 +106,33 @@ def test_workspace_size(pa):
     assert pa.pa_split_workspace_size(ctypes.byref(shp), 50000, 500) == 0
 
 
+@pytest.mark.parametrize("hq,hkv,d,max_q,want_chunks", [
+    (32, 8, 128, 512, 16),      # G = 4: 32 tokens per tcgen05 CTA
+    (64, 8, 128, 700, 44),      # G = 8: 16 tokens, a ragged last chunk
+    (8, 8, 128, 129, 2),        # G = 1: 128 tokens
+    (32, 8, 128, 31, 0),        # a chunk that cannot fill 128 rows: mma.sync kernel
+    (8, 2, 64, 512, 0),         # head_dim 64: mma.sync kernel
+    (12, 2, 128, 512, 0),       # G = 6: mma.sync kernel
+])
+def test_prefill_workspace_size(pa, hq, hkv, d, max_q, want_chunks):
+    """One int32 per (sequence, chunk) item of the tcgen05 kernel, rounded up to
+    256 bytes; 0 where pa_prefill takes the mma.sync kernel."""
+    shp = _shape(num_seqs=5, num_q_heads=hq, num_kv_heads=hkv, head_dim=d)
+    want = -(-5 * want_chunks * 4 // 256) * 256
+    assert pa.pa_prefill_workspace_size(ctypes.byref(shp), max_q) == want
+    assert pa.pa_prefill_workspace_size(ctypes.byref(shp), 0) == 0
+    assert pa.pa_prefill_workspace_size(None, max_q) == 0
+
+
+def test_prefill_ws_argument_checks(pa):
+    shp = _shape(num_seqs=2, num_q_heads=32, num_kv_heads=8)
+    # a workspace smaller than the size query asks for, or misaligned
+    for ws, n in ((FAKE, 16), (ctypes.c_void_p((1 << 20) + 4), 4096)):
+        st = pa.pa_prefill_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 512, ws, n, FAKE,
+                              ctypes.byref(shp), None)
+        assert st == lib.PA_ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         lib.load(str(tmp_path / "missing.so"))
