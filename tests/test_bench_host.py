@@ -54,3 +54,36 @@ def test_whole_job_value_counts_all_ranks():
     import bench
     assert bench.whole_job_gbs(1_000_000_000, 4, 2.0) == pytest.approx(2000.0)
     assert bench.max_over_ranks(3.5) == 3.5       # no process group: identity
+
+
+def test_prefill_flops_counts_every_attended_key():
+    """The closed form in bench.prefill_flops against a count over every new
+    token's position (4 D FLOPs per query head per attended key)."""
+    import bench
+    from paged_kv_cache_226_gb300 import inputs as pin
+    w = pin.build_prefill_workload(params=dict(dtype="bf16", lens=[1, 17, 300, 64, 5],
+                                               chunks=[1, 17, 29, 0, 3], num_q_heads=8,
+                                               num_kv_heads=2, head_dim=64, block_size=16),
+                                   seed=5)
+    attended = 0
+    for L, C in zip(w.context_lens.tolist(), (w.query_start[1:] - w.query_start[:-1]).tolist()):
+        for i in range(C):
+            attended += (L - C + i) + 1            # keys 0 .. position of new token i
+    assert bench.prefill_flops(w) == 4 * 64 * 8 * attended
+
+
+def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
+    """A committed DRAM-traffic figure is reported only while the kernel's
+    sources hash to the value it was captured on."""
+    import json
+    import bench
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = {"source_sha256_16": bench.source_hash("paged_prefill"), "dram_bytes_per_launch": 1234}
+    (prof / "paged_prefill_w.json").write_text(json.dumps(rec))
+    assert bench.profiled_traffic("w", "paged_prefill") == 1234
+    rec["source_sha256_16"] = "0" * 16
+    (prof / "paged_prefill_w.json").write_text(json.dumps(rec))
+    assert bench.profiled_traffic("w", "paged_prefill") is None
+    assert bench.profiled_traffic("absent", "paged_prefill") is None
