@@ -161,14 +161,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) return false;
         if (lane < nbox && (blk < 0 || blk >= p.num_blocks)) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+        // lane i issues box i's two halves itself (the bytes to expect were
+        // registered by lane 0 above, earlier in this warp's program order):
+        // two warp instructions per tile instead of sixteen single-lane ones
         uint8_t* dst = smem + kind_off + s * kTcOperand;
-        for (int i = 0; i < nbox; ++i) {
-            const int bi = __shfl_sync(0xffffffffu, blk, i);
-            const int si = __shfl_sync(0xffffffffu, sub, i);
-            if (lane == 0) {
-                tma_load_4d(dst + i * kBox16Bytes, map, &full[s], 0, g, si, bi);
-                tma_load_4d(dst + kTcHalf + i * kBox16Bytes, map, &full[s], kBoxElems, g, si, bi);
-            }
+        if (lane < nbox) {
+            tma_load_4d(dst + lane * kBox16Bytes, map, &full[s], 0, g, sub, blk);
+            tma_load_4d(dst + kTcHalf + lane * kBox16Bytes, map, &full[s], kBoxElems, g, sub, blk);
         }
         return true;
     };
