@@ -325,6 +325,181 @@ def bench_reference(args):
     return 0
 
 
+def decode_setup(w: pin.Workload, dev, mode: str, partition: int, kv_dtype: str, fp8_seed: int):
+    """Device inputs and the marshalled layer-step (lib.StepPlan) of a
+    workload; with kv_dtype "fp8" the pools are replaced by E4M3 codes."""
+    max_len = int(w.context_lens.max())
+    kc, vc, scales = w.k_cache, w.v_cache, {}
+    if kv_dtype == "fp8":
+        if mode not in ("fused", "balanced"):
+            raise SystemExit("--kv-dtype fp8 runs the fused steps")
+        if w.k_cache.is_cuda:
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(fp8_seed)
+            kc = pin.fp8_codes_device(gen, tuple(w.k_cache.shape), FP8_K_SCALE, dev)
+            vc = pin.fp8_codes_device(gen, tuple(w.v_cache.shape), FP8_V_SCALE, dev)
+        else:
+            rng = np.random.default_rng(fp8_seed)
+            kc = pin.fp8_codes(rng, tuple(w.k_cache.shape), FP8_K_SCALE)
+            vc = pin.fp8_codes(rng, tuple(w.v_cache.shape), FP8_V_SCALE)
+        scales = dict(k_scale=FP8_K_SCALE, v_scale=FP8_V_SCALE)
+    d = {k: v.to(dev) for k, v in dict(
+        q=w.q, k_new=w.k_new, v_new=w.v_new, k_cache=kc, v_cache=vc,
+        block_tables=torch.from_numpy(w.block_tables),
+        context_lens=torch.from_numpy(w.context_lens),
+        slot_mapping=torch.from_numpy(w.slot_mapping)).items()}
+    plan = lib.StepPlan(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
+                        d["v_cache"], d["block_tables"], d["context_lens"], w.scale, max_len,
+                        mode=mode, partition_size=partition, **scales)
+    nb = step_bytes(w, mode, partition, 1 if kv_dtype == "fp8" else 2)
+    return d, plan, nb
+
+
+def time_steps(plan, flush, dev, stream, steps: int, warmup: int, gpu_index: int, world: int):
+    """Warm-up, then the timed region.  Phase 1 (the K timed steps): events
+    only at step boundaries, so consecutive kernels of a step overlap their
+    launch latency (programmatic dependent launch).  Phase 2 (kernel
+    attribution, min(K, 1000) more steps): events between the kernels as
+    well, which serialises them, to time each kernel for the roofline.
+    Returns per-step and per-kernel milliseconds and the clocks seen."""
+    for _ in range(warmup):
+        flush(1.0)
+        run_step(plan)
+    torch.cuda.synchronize(dev)
+    assert lib.read_device_errors(dev) == 0
+    n_attr = min(steps, 1000)
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_attr)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_index) as clk:
+        time.sleep(0.4)
+        t_epoch0 = time.time()
+        t_wall = time.perf_counter()
+        # Hold the GPU briefly so the host queues the steps ahead of it: the
+        # events then see only GPU time, not Python launch overhead.
+        torch.cuda._sleep(int(2e7))
+        for i in range(steps):
+            flush(float(i))
+            step_ev[i][0].record(stream)
+            run_step(plan)
+            step_ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+        torch.cuda._sleep(int(2e7))
+        for i in range(n_attr):
+            flush(float(i))
+            run_step(plan, evs[i], stream)
+        torch.cuda.synchronize(dev)
+        t_epoch1 = time.time()
+        time.sleep(0.1)
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[1]) for e in step_ev]
+    return {"step_ms": step_ms,
+            "k1_ms": [e[0].elapsed_time(e[1]) for e in evs],
+            "k2_ms": [e[1].elapsed_time(e[2]) for e in evs],
+            "k3_ms": [e[2].elapsed_time(e[3]) for e in evs],
+            "serial_ms": sum(e[0].elapsed_time(e[3]) for e in evs) / n_attr,
+            "n_attr": n_attr, "t_wall": t_wall, "clocks": clk.summary(t_epoch0, t_epoch1)}
+
+
+DOMINANT = {"split": "paged_decode_split", "single": "paged_decode",
+            "fused": "paged_decode_step", "balanced": "balanced_step"}
+LAUNCHES_PER_STEP = {"split": 3, "single": 2, "fused": 1, "balanced": 2}
+
+
+def decode_summary(w: pin.Workload, mode: str, partition: int, kv_dtype: str, nb: dict,
+                   tm: dict, dev, world: int, hbm: float, peak_src: str, traffic_key: str):
+    """Step time statistics, per-kernel times and the dominant kernel's
+    roofline of one timed decode workload."""
+    ms = max_over_ranks(sum(tm["step_ms"]) / len(tm["step_ms"]), dev)
+    ms_median = max_over_ranks(float(np.median(tm["step_ms"])), dev)
+    ms_p99 = max_over_ranks(float(np.percentile(tm["step_ms"], 99)), dev)
+    dom = DOMINANT[mode]
+    dom_ms = sum(tm["k2_ms"]) / len(tm["k2_ms"])
+    dom_bytes = nb["kernels"][dom]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    kern = {dom: round(1e3 * dom_ms, 2)}
+    if mode not in ("fused", "balanced"):
+        kern["reshape_and_cache"] = round(1e3 * sum(tm["k1_ms"]) / len(tm["k1_ms"]), 2)
+    if mode == "split":
+        kern["lse_reduce"] = round(1e3 * sum(tm["k3_ms"]) / len(tm["k3_ms"]), 2)
+    kern["note"] = (f"event-bracketed, serialised, over {tm['n_attr']} more steps; the same "
+                    f"step serialised takes {1e3 * tm['serial_ms']:.2f} us")
+    value = whole_job_gbs(nb["layer_step"], world, ms)
+    return {
+        "value": round(value, 3), "unit": "GB/s", "ms_per_step": round(ms, 5),
+        "us_per_layer_step": round(ms * 1e3, 2),
+        "us_per_layer_step_median": round(ms_median * 1e3, 2),
+        "us_per_layer_step_p99": round(ms_p99 * 1e3, 2),
+        "hbm_frac_of_measured" if peak_src == "measured" else "hbm_frac_of_fallback":
+            round(value / world / hbm, 4),
+        "mode": mode, "partition_tokens": partition if mode != "single" else None,
+        "kv_dtype": w.dtype if kv_dtype != "fp8" else "e4m3",
+        "kv_bytes": nb["kv"],
+        "kv_bytes_unique": int(w.kv_bytes_unique() * (1 if kv_dtype != "fp8" else 0.5)),
+        "bytes_per_step": nb["layer_step"],
+        "kernels_us": kern,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2),
+                     "peak": hbm, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "traffic": profiled_traffic(traffic_key, dom)},
+        "clocks": tm["clocks"],
+        "gpu_launches": LAUNCHES_PER_STEP[mode] * len(tm["step_ms"]),
+    }
+
+
+# Further workloads timed in the same run (N = 1) and reported under
+# "configs": name -> (workload, mode, partition tokens (0: chosen from the
+# batch shape), cache type).
+SUB_CONFIGS = {
+    "llama8b_split512": ("llama8b", "split", 512, "auto"),
+    "llama8b_fp8": ("llama8b", "fused", 0, "fp8"),
+    "prefix": ("prefix", "fused", 0, "auto"),
+    "llama70b": ("llama70b", "fused", 0, "auto"),
+    "long16": ("long16", "fused", 0, "auto"),
+    "long16_split512": ("long16", "split", 512, "auto"),
+    "long32": ("long32", "fused", 0, "auto"),
+    "long32_split512": ("long32", "split", 512, "auto"),
+    "prefill8b": ("prefill8b", "prefill", 0, "auto"),
+}
+
+
+def bench_sub_configs(names, args, dev, stream, flush, hbm, peak_src):
+    """Each named workload built with its pools drawn on the device, timed
+    like the headline (same steps, warm-up and L2 flush), then freed."""
+    out = {}
+    for name in names:
+        cfg, mode, partition, kv_dtype = SUB_CONFIGS[name]
+        t0 = time.perf_counter()
+        if mode == "prefill":
+            res = time_prefill(cfg, dev, args.steps, args.warmup, 0, flush, stream)
+            res.pop("metric", None)
+            out[name] = res
+        else:
+            w = pin.build_workload(cfg, seed=rank_seed(cfg, 0), pool_device=dev)
+            max_len = int(w.context_lens.max())
+            p = partition or lib.choose_partition(w.num_seqs, w.num_kv_heads, max_len,
+                                                  w.block_size, dev)
+            d, plan, nb = decode_setup(w, dev, mode, p, kv_dtype, rank_seed(cfg, 0) + 7)
+            tm = time_steps(plan, flush, dev, stream, args.steps, args.warmup, dev.index or 0, 1)
+            res = decode_summary(w, mode, p, kv_dtype, nb, tm, dev, 1, hbm, peak_src,
+                                 cfg + ("_fp8" if kv_dtype == "fp8" else ""))
+            res["workload"] = f"{cfg}: {pin.DESCRIPTIONS[cfg]}"
+            res["device_errors"] = lib.read_device_errors(dev)
+            out[name] = res
+            del d, plan, w
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        out[name]["build_and_time_s"] = round(time.perf_counter() - t0, 2)
+    return out
+
+
 def bench_ours(args):
     rank, world, local_rank = dist_env()
     if not torch.cuda.is_available():
@@ -342,77 +517,11 @@ def bench_ours(args):
     mode = args.mode if args.mode != "auto" else "fused"
     partition = args.partition or lib.choose_partition(w.num_seqs, w.num_kv_heads, max_len,
                                                        w.block_size, dev)
-    S = lib.num_partitions(max_len, partition)
-
-    kc, vc, scales = w.k_cache, w.v_cache, {}
-    if args.kv_dtype == "fp8":
-        if mode not in ("fused", "balanced"):
-            raise SystemExit("--kv-dtype fp8 runs the fused steps")
-        rng = np.random.default_rng(rank_seed(args.config, rank) + 7)
-        kc = pin.fp8_codes(rng, tuple(w.k_cache.shape), FP8_K_SCALE)
-        vc = pin.fp8_codes(rng, tuple(w.v_cache.shape), FP8_V_SCALE)
-        scales = dict(k_scale=FP8_K_SCALE, v_scale=FP8_V_SCALE)
-    d = {k: v.to(dev) for k, v in dict(
-        q=w.q, k_new=w.k_new, v_new=w.v_new, k_cache=kc, v_cache=vc,
-        block_tables=torch.from_numpy(w.block_tables),
-        context_lens=torch.from_numpy(w.context_lens),
-        slot_mapping=torch.from_numpy(w.slot_mapping)).items()}
-    plan = lib.StepPlan(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
-                        d["v_cache"], d["block_tables"], d["context_lens"], w.scale, max_len,
-                        mode=mode, partition_size=partition, **scales)
+    d, plan, nb = decode_setup(w, dev, mode, partition, args.kv_dtype,
+                               rank_seed(args.config, rank) + 7)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
-    nb = step_bytes(w, mode, partition, 1 if args.kv_dtype == "fp8" else 2)
-
-    for _ in range(args.warmup):
-        flush(1.0)
-        run_step(plan)
-    torch.cuda.synchronize(dev)
-    assert lib.read_device_errors(dev) == 0
-
-    # Timed region.  Phase 1 (the K timed steps): events only at step
-    # boundaries, so consecutive kernels of a step overlap their launch
-    # latency (programmatic dependent launch).  Phase 2 (kernel attribution,
-    # min(K, 1000) more steps): events between the kernels as well, which
-    # serialises them, to time each kernel for the roofline.
-    n_attr = min(args.steps, 1000)
-    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_attr)]
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local_rank) as clk:
-        time.sleep(0.4)
-        t_epoch0 = time.time()
-        t_wall = time.perf_counter()
-        # Hold the GPU briefly so the host queues the steps ahead of it: the
-        # events then see only GPU time, not Python launch overhead.
-        torch.cuda._sleep(int(2e7))
-        for i in range(args.steps):
-            flush(float(i))
-            step_ev[i][0].record(stream)
-            run_step(plan)
-            step_ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall
-        torch.cuda._sleep(int(2e7))
-        for i in range(n_attr):
-            flush(float(i))
-            run_step(plan, evs[i], stream)
-        torch.cuda.synchronize(dev)
-        t_epoch1 = time.time()
-        time.sleep(0.1)
-    if world > 1:
-        dist.barrier()
-    step_ms = [e[0].elapsed_time(e[1]) for e in step_ev]
-    k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    k3_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    serial_ms = sum(e[0].elapsed_time(e[3]) for e in evs) / n_attr
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
-    ms_median = max_over_ranks(float(np.median(step_ms)), dev)
-    ms_p99 = max_over_ranks(float(np.percentile(step_ms, 99)), dev)
+    tm = time_steps(plan, flush, dev, stream, args.steps, args.warmup, local_rank, world)
     errs = lib.read_device_errors(dev)
 
     # End to end through the public API: every step copies its inputs from
@@ -457,62 +566,59 @@ def bench_ours(args):
                "copies_per_step": "1 host-to-device (inputs packed), 1 device-to-host (out), "
                                   "each a short kernel on pinned host memory (pa_copy_async)",
                "launch": "one CUDA graph per step (upload, layer-step, read-back)"}
+        del plan_e2e, stage
 
+    hbm, peak_src = peaks()
+    summ = decode_summary(w, mode, partition, args.kv_dtype, nb, tm, dev, world, hbm, peak_src,
+                          args.config + ("_fp8" if args.kv_dtype == "fp8" else ""))
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
 
-    hbm, peak_src = peaks()
-    dom = {"split": "paged_decode_split", "single": "paged_decode",
-           "fused": "paged_decode_step", "balanced": "balanced_step"}[mode]
-    dom_ms = sum(k2_ms) / len(k2_ms)
-    dom_bytes = nb["kernels"][dom]
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    value = whole_job_gbs(nb["layer_step"], world, ms)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
+    configs = None
+    if world == 1 and args.configs != "none":
+        names = list(SUB_CONFIGS) if args.configs == "all" else \
+            [n for n in args.configs.split(",") if n]
+        del d, plan
+        torch.cuda.empty_cache()
+        configs = bench_sub_configs(names, args, dev, stream, flush, hbm, peak_src)
+    frac_key = "hbm_frac_of_measured" if peak_src == "measured" else "hbm_frac_of_fallback"
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-        "us_per_layer_step": round(ms * 1e3, 2),
-        "us_per_layer_step_median": round(ms_median * 1e3, 2),
-        "us_per_layer_step_p99": round(ms_p99 * 1e3, 2),
-        "hbm_frac_of_measured" if peak_src == "measured" else "hbm_frac_of_fallback":
-            round(value / world / hbm, 4),
+        "metric": METRIC, "value": summ["value"], "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": summ["ms_per_step"],
+        "us_per_layer_step": summ["us_per_layer_step"],
+        "us_per_layer_step_median": summ["us_per_layer_step_median"],
+        "us_per_layer_step_p99": summ["us_per_layer_step_p99"],
+        frac_key: summ[frac_key],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype if args.kv_dtype != "fp8" else f"{w.dtype} (q, out), e4m3 (K/V cache)",
         "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
         "config": {"workload": f"{w.name}: {pin.DESCRIPTIONS[w.name]}"
                                + (f" with {args.params}" if args.params else ""), "mode": mode,
-                   "partition_tokens": partition if mode != "single" else None,
+                   "partition_tokens": summ["partition_tokens"],
                    "l2": "flushed before every step (256 MiB write, then 256 MiB read of another "
                          "buffer; outside the step's events)",
-                   "kv_bytes": nb["kv"], "kv_bytes_unique": w.kv_bytes_unique() * (
-                       1 if args.kv_dtype != "fp8" else 0.5),
-                   "bytes_per_step": nb["layer_step"], "seqs_per_gpu": w.num_seqs},
-        "kernels_us": {**({} if mode in ("fused", "balanced") else
-                          {"reshape_and_cache": round(1e3 * sum(k1_ms) / len(k1_ms), 2)}),
-                       dom: round(1e3 * dom_ms, 2),
-                       "note": f"event-bracketed, serialised, over {n_attr} more steps; the "
-                               f"same step serialised takes {1e3 * serial_ms:.2f} us"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2),
-                     "peak": hbm, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "algorithmic_bytes_per_launch": dom_bytes,
-                     "traffic": profiled_traffic(
-                         args.config + ("_fp8" if args.kv_dtype == "fp8" else ""), dom)},
-        "clocks": clk.summary(t_epoch0, t_epoch1),
-        "gpu_launches": {"split": 3, "single": 2, "fused": 1, "balanced": 2}[mode] * args.steps,
+                   "kv_bytes": summ["kv_bytes"], "kv_bytes_unique": summ["kv_bytes_unique"],
+                   "bytes_per_step": summ["bytes_per_step"], "seqs_per_gpu": w.num_seqs},
+        "kernels_us": summ["kernels_us"],
+        "roofline": summ["roofline"],
+        "clocks": summ["clocks"],
+        "gpu_launches": summ["gpu_launches"],
         "device_errors": errs,
-        "wall_s_timed": round(t_wall, 4),
+        "wall_s_timed": round(tm["t_wall"], 4),
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
-    if mode == "split":
-        line["kernels_us"]["lse_reduce"] = round(1e3 * sum(k3_ms) / len(k3_ms), 2)
+    if configs is not None:
+        line["configs"] = configs
+        line["configs_note"] = (
+            "further workloads timed in the same run, each with its pools drawn on the device "
+            "by a seeded generator; same steps, warm-up and L2 flush as the headline; not in "
+            "value, gpu_launches or wall_s_timed")
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -585,19 +691,12 @@ def prefill_flops(w) -> int:
     return int(4 * w.head_dim * w.num_q_heads * attended)
 
 
-def bench_prefill(args):
-    """Chunked-prefill attention (pa_prefill) over the paged cache: every new
-    token of every sequence attends causally through its block table."""
-    rank, world, local_rank = dist_env()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    pa_build.build()
-    lib.load()
-    w = pin.build_prefill_workload(args.prefill_config,
-                                   seed=pin.PREFILL_CONFIGS[args.prefill_config][0] + 1000 * rank)
+def time_prefill(name: str, dev, steps: int, warmup: int, rank: int, flush, stream,
+                 world: int = 1):
+    """Chunked-prefill attention (pa_prefill) over the paged cache, every new
+    token of every sequence attending causally through its block table:
+    timed with CUDA events around each call, L2 flushed before each call."""
+    w = pin.build_prefill_workload(name, seed=pin.PREFILL_CONFIGS[name][0] + 1000 * rank)
     d = {k: v.to(dev) if isinstance(v, torch.Tensor) else torch.from_numpy(v).to(dev)
          for k, v in dict(q=w.q, kn=w.k_new, vn=w.v_new, kc=w.k_cache, vc=w.v_cache,
                           bt=w.block_tables, cl=w.context_lens, qs=w.query_start,
@@ -605,8 +704,6 @@ def bench_prefill(args):
     lib.reshape_and_cache(d["kn"], d["vn"], d["sm"], d["kc"], d["vc"])
     max_q = int(np.diff(w.query_start).max())
     out = torch.empty_like(d["q"])
-    flush = L2Flush(dev)
-    stream = torch.cuda.current_stream(dev)
     shp = lib.make_shape(w.num_seqs, d["q"].shape[1], d["kc"], d["bt"].shape[1])
     ws_bytes = lib.prefill_workspace_size(shp, max_q)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
@@ -616,21 +713,21 @@ def bench_prefill(args):
         lib.prefill(d["q"], d["kc"], d["vc"], d["bt"], d["cl"], d["qs"], w.scale, max_q, out,
                     workspace=ws)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush(1.0)
         call()
     torch.cuda.synchronize(dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     import torch.distributed as dist
     sync_ranks = dist.is_available() and dist.is_initialized()
-    with ClockSampler(local_rank) as clocks:
+    with ClockSampler(dev.index or 0) as clocks:
         time.sleep(0.2)
         if sync_ranks:
             dist.barrier()
         torch.cuda.synchronize(dev)
         t_start = time.time()
-        for i in range(args.steps):
+        for i in range(steps):
             flush(float(i))
             evs[i][0].record(stream)
             call()
@@ -641,31 +738,61 @@ def bench_prefill(args):
             dist.barrier()
         time.sleep(0.2)
     clk = clocks.summary(t_start, t_end)
-    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, dev)
+    times = [a.elapsed_time(b) for a, b in evs]
+    ms = max_over_ranks(sum(times) / steps, dev)
     flops = prefill_flops(w)
     tflops = flops * world / (ms * 1e-3) / 1e12
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         peak = float(json.load(f)["bf16_tflops"])
     kv_tokens = int(w.context_lens.sum())
     kv_bytes = kv_tokens * w.num_kv_heads * w.head_dim * 2 * 2
-    line = {"metric": "chunked-prefill attention TFLOP/s over the paged cache",
-            "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.dtype, "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
-            "config": {"workload": f"{w.name}: {pin.PREFILL_DESCRIPTIONS[w.name]}",
-                       "new_tokens": int(w.query_start[-1]), "kv_tokens": kv_tokens,
-                       "kv_bytes": kv_bytes, "flops_per_call": flops,
-                       "l2": "flushed before every call (outside its events)"},
-            "roofline": {"bound": "tensor", "kernel": "paged_prefill", "achieved": round(tflops / world, 2),
+    return {"metric": "chunked-prefill attention TFLOP/s over the paged cache",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+            "us_per_call_median": round(1e3 * float(np.median(times)), 2),
+            "us_per_call_p99": round(1e3 * float(np.percentile(times, 99)), 2),
+            "dtype": w.dtype,
+            "workload": f"{w.name}: {pin.PREFILL_DESCRIPTIONS[w.name]}",
+            "new_tokens": int(w.query_start[-1]), "kv_tokens": kv_tokens,
+            "kv_bytes": kv_bytes, "flops_per_call": flops,
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill",
+                         "achieved": round(tflops / world, 2),
                          "peak": peak, "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, "
                                                       "burst; tcgen05 kernel, kernel='auto')",
                          "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4),
-                         "traffic": profiled_traffic(args.prefill_config, "paged_prefill")},
-            "clocks": clk, "gpu_launches": args.steps * launches_per_call,
+                         "traffic": profiled_traffic(name, "paged_prefill")},
+            "clocks": clk, "gpu_launches": steps * launches_per_call,
             "device_errors": lib.read_device_errors(dev)}
+
+
+def bench_prefill(args):
+    """The chunked-prefill bench line (--op prefill)."""
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pa_build.build()
+    lib.load()
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    r = time_prefill(args.prefill_config, dev, args.steps, args.warmup, rank, flush, stream,
+                     world)
+    line = {"metric": r["metric"], "value": r["value"], "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": r["dtype"], "data": "synthetic (seeded N(0,1) q/K/V, seeded block placement)",
+            "config": {"workload": r["workload"], "new_tokens": r["new_tokens"],
+                       "kv_tokens": r["kv_tokens"], "kv_bytes": r["kv_bytes"],
+                       "flops_per_call": r["flops_per_call"],
+                       "l2": "flushed before every call (outside its events)"},
+            "roofline": r["roofline"], "clocks": r["clocks"],
+            "gpu_launches": r["gpu_launches"], "device_errors": r["device_errors"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
     return 0
 
 
@@ -689,6 +816,10 @@ def main(argv=None):
                     help="cache element type: the workload's fp16/bf16, or E4M3 codes")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default="all",
+                    help="further workloads timed after the headline at N = 1 and reported "
+                         "under \"configs\": all, none, or a comma list of " +
+                         ", ".join(SUB_CONFIGS))
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)        # at least 3 untimed warm-up steps
     if args.impl == "reference":

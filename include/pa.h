@@ -348,13 +348,17 @@ int pa_copy_blocks(const void* k_src, const void* v_src, int64_t src_num_blocks,
  *
  * Set-up: the first call on a device (with that device current) looks up the
  * buffer's device address; make that first call before any stream capture.
+ * The address belongs to the CUDA context it was looked up in: a call under
+ * another context (a driver-API context made current by the caller, or the
+ * primary context created anew after cudaDeviceReset) looks it up again, so
+ * the first call under each new context must also come before any capture.
  *
  * Sharing: every call on a device uses the same buffer, which keeps the last
  * call's contents (nothing in it needs to start at zero).  Calls whose work
  * overlaps on the GPU -- e.g. issued on two streams without ordering between
  * them -- race on the buffer and corrupt each other's results; order them.
- * Errors are those of pa_decode_split and pa_reduce, plus PA_ERR_WORKSPACE
- * for the limit above.
+ * Errors: the argument checks of pa_decode_split and pa_reduce run first and
+ * give the same statuses; then PA_ERR_WORKSPACE for the limit above.
  */
 int pa_decode_static_workspace(const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_tables, const int32_t* context_lens,

@@ -14,7 +14,15 @@ namespace {
 __device__ int g_device_errors;
 
 constexpr int kMaxDevices = 64;
-int* g_err_ptr[kMaxDevices];
+// Its address, looked up per device and remembered with the context it was
+// looked up in: a __device__ variable's address belongs to a context, so a
+// different current context (a driver-API context, or the primary context
+// re-created after cudaDeviceReset) triggers a fresh lookup.
+struct SymbolSlot {
+    void* ctx;
+    int* ptr;
+};
+SymbolSlot g_err_slot[kMaxDevices];
 std::mutex g_err_mutex;
 thread_local int t_last_cuda_error = 0;
 
@@ -23,20 +31,32 @@ int cuda_fail(cudaError_t e) {
     return PA_ERR_CUDA;
 }
 
+// cuCtxGetCurrent through the runtime's driver entry point (no link
+// dependency on libcuda).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn g_ctx_get = nullptr;
+std::once_flag g_ctx_once;
+cudaError_t g_ctx_status = cudaSuccess;
+
 // Device address of the error word on the current device.
 cudaError_t error_word(int** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* ctx = nullptr;
+    if ((e = pa::current_context(&ctx)) != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_err_mutex);
-    if (g_err_ptr[dev] == nullptr) {
+    SymbolSlot& slot = g_err_slot[dev];
+    if (slot.ptr == nullptr || ctx == nullptr || slot.ctx != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_device_errors);
+        e = cudaGetSymbolAddress(&p, g_device_errors);   // makes a context current if none is
         if (e != cudaSuccess) return e;
-        g_err_ptr[dev] = static_cast<int*>(p);
+        if ((e = pa::current_context(&ctx)) != cudaSuccess) return e;
+        slot.ctx = ctx;
+        slot.ptr = static_cast<int*>(p);
     }
-    *out = g_err_ptr[dev];
+    *out = slot.ptr;
     return cudaSuccess;
 }
 
@@ -160,6 +180,40 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 
 void pa::record_cuda_error(int cuda_error) { t_last_cuda_error = cuda_error; }
+
+cudaError_t pa::current_context(void** ctx) {
+    std::call_once(g_ctx_once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e == cudaSuccess && (q != cudaDriverEntryPointSuccess || p == nullptr))
+            e = cudaErrorSymbolNotFound;
+        g_ctx_status = e;
+        g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    if (g_ctx_status != cudaSuccess) return g_ctx_status;
+    CUcontext c = nullptr;
+    if (g_ctx_get(&c) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;   // "invalid device context"
+    *ctx = static_cast<void*>(c);
+    return cudaSuccess;
+}
+
+int pa::check_split_request(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            int32_t partition_size, int32_t max_num_partitions, const void* out,
+                            const pa_shape* shp) {
+    // the checks of pa_decode_split (16-bit cache), then those of pa_reduce
+    // on its output, in the order those entry points run them
+    int st = check_decode_args(q, k_cache, v_cache, block_tables, context_lens, shp);
+    if (st != PA_OK) return st;
+    if (partition_size <= 0 || partition_size % shp->block_size != 0) return PA_ERR_INVALID_ARG;
+    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
+    if (max_num_partitions > 65535) return PA_ERR_UNSUPPORTED;
+    if (shp->num_seqs == 0) return PA_OK;
+    if (!out || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
 
 extern "C" {
 

@@ -180,4 +180,14 @@ cudaError_t launch_copy_blocks(const void* k_src, const void* v_src, int64_t src
 // Sets the value pa_last_cuda_error() reports on this host thread.
 void record_cuda_error(int cuda_error);
 
+// The calling thread's current CUDA context (cuCtxGetCurrent; null if none).
+cudaError_t current_context(void** ctx);
+
+// Argument checks of pa_decode_split + pa_reduce on a 16-bit cache, apart
+// from the workspace pointers: PA_OK or the status those entry points return.
+int check_split_request(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        int32_t partition_size, int32_t max_num_partitions, const void* out,
+                        const pa_shape* shp);
+
 }  // namespace pa

@@ -22,27 +22,41 @@ namespace {
 __device__ __align__(256) unsigned char g_static_workspace[PA_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_workspace_ptr[kMaxDevices];
+// The buffer's device address per device, with the context it was looked up
+// in: a __device__ array's address belongs to a CUDA context, so a call made
+// under another context (a driver-API context, or the primary context made
+// anew after cudaDeviceReset) looks it up again instead of reusing an
+// address that context never mapped.
+struct Slot {
+    void* ctx;
+    void* ptr;
+};
+Slot g_workspace_slot[kMaxDevices];
 std::mutex g_workspace_mutex;
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Device address of the buffer on the current device.  The first call on a
-// device looks it up (cudaGetSymbolAddress, which also loads the module
-// holding the buffer); later calls reuse the cached address.
+// Device address of the buffer on the current device and context.  The
+// first call there looks it up (cudaGetSymbolAddress, which also loads the
+// module holding the buffer); later calls under the same context reuse it.
 cudaError_t workspace_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* ctx = nullptr;
+    if ((e = pa::current_context(&ctx)) != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_workspace_mutex);
-    if (g_workspace_ptr[dev] == nullptr) {
+    Slot& slot = g_workspace_slot[dev];
+    if (slot.ptr == nullptr || ctx == nullptr || slot.ctx != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_workspace);
         if (e != cudaSuccess) return e;
-        g_workspace_ptr[dev] = p;
+        if ((e = pa::current_context(&ctx)) != cudaSuccess) return e;   // made current above
+        slot.ctx = ctx;
+        slot.ptr = p;
     }
-    *out = g_workspace_ptr[dev];
+    *out = slot.ptr;
     return cudaSuccess;
 }
 
@@ -53,10 +67,11 @@ extern "C" int pa_decode_static_workspace(const void* q, const void* k_cache,
                                           const int32_t* context_lens, float scale,
                                           int32_t partition_size, int32_t max_num_partitions,
                                           void* out, const pa_shape* shp, void* stream) {
-    if (shp == nullptr || partition_size <= 0) return PA_ERR_INVALID_ARG;
-    if (max_num_partitions <= 0) return PA_ERR_WORKSPACE;
-    if (shp->num_seqs < 0 || shp->num_q_heads <= 0 || shp->head_dim <= 0)
-        return PA_ERR_INVALID_ARG;
+    // the argument checks of pa_decode_split + pa_reduce come first, so a
+    // malformed request gets the status those entry points give it
+    const int st0 = pa::check_split_request(q, k_cache, v_cache, block_tables, context_lens,
+                                            partition_size, max_num_partitions, out, shp);
+    if (st0 != PA_OK) return st0;
     if (shp->num_seqs == 0) return PA_OK;
     // tmp_out [B][Hq][S][D], then max_logits and exp_sums [B][Hq][S], fp32,
     // each part starting on a 256-byte boundary.

@@ -232,6 +232,20 @@ def normal_tensor(rng: np.random.Generator, shape, dtype: str,
     return out.view(*shape)
 
 
+def normal_tensor_device(gen: torch.Generator, shape, dtype: str, device,
+                         chunk_elems: int = 1 << 26) -> torch.Tensor:
+    """N(0,1) float32 draws of a seeded device generator rounded to
+    nearest-even 16-bit, made on the device (large pools for timing runs,
+    where the host draw would take tens of seconds)."""
+    out = torch.empty(tuple(shape), dtype=_TORCH_DTYPES[dtype], device=device)
+    flat = out.view(-1)
+    for s in range(0, flat.numel(), chunk_elems):
+        e = min(flat.numel(), s + chunk_elems)
+        flat[s:e] = torch.randn(e - s, generator=gen, device=device,
+                                dtype=torch.float32).to(out.dtype)
+    return out
+
+
 # ----------------------------------------------------------------------------
 # workloads
 # ----------------------------------------------------------------------------
@@ -338,7 +352,8 @@ def _draw_lengths(rng: np.random.Generator, p: dict) -> (np.ndarray, int):
 
 
 def build_workload(name: Optional[str] = None, seed: Optional[int] = None,
-                   params: Optional[dict] = None, pool_slack: float = 0.10) -> Workload:
+                   params: Optional[dict] = None, pool_slack: float = 0.10,
+                   pool_device=None) -> Workload:
     """Build one named configuration (or ``params`` for a custom one).
 
     Recipe (seeded numpy PCG64): context lengths, then the pool permutation,
@@ -347,6 +362,11 @@ def build_workload(name: Optional[str] = None, seed: Optional[int] = None,
     its first ``L_b - 1`` tokens; its last token is appended with
     ``append_token`` and its slot goes to ``slot_mapping``.  Table rows are
     padded with block id 0 past their end.
+
+    With ``pool_device`` the two pools are drawn instead on that device by a
+    torch generator seeded with ``seed`` (same distribution, other values;
+    everything else is unchanged) and returned there: timing runs of the
+    large workloads use it.
     """
     if params is None:
         base_seed, params = CONFIGS[name]
@@ -390,8 +410,14 @@ def build_workload(name: Optional[str] = None, seed: Optional[int] = None,
     q = normal_tensor(rng, (B, hq, d), dt)
     k_new = normal_tensor(rng, (B, hkv, d), dt)
     v_new = normal_tensor(rng, (B, hkv, d), dt)
-    k_cache = normal_tensor(rng, (nb, bs, hkv, d), dt)
-    v_cache = normal_tensor(rng, (nb, bs, hkv, d), dt)
+    if pool_device is None:
+        k_cache = normal_tensor(rng, (nb, bs, hkv, d), dt)
+        v_cache = normal_tensor(rng, (nb, bs, hkv, d), dt)
+    else:
+        gen = torch.Generator(device=pool_device)
+        gen.manual_seed(seed)
+        k_cache = normal_tensor_device(gen, (nb, bs, hkv, d), dt, pool_device)
+        v_cache = normal_tensor_device(gen, (nb, bs, hkv, d), dt, pool_device)
     return Workload(name=name, dtype=dt, num_seqs=B, num_q_heads=hq, num_kv_heads=hkv,
                     head_dim=d, block_size=bs, num_blocks=nb, scale=1.0 / math.sqrt(d),
                     context_lens=lens.astype(np.int32), block_tables=tables,
@@ -406,6 +432,20 @@ def fp8_codes(rng: np.random.Generator, shape, scale: float) -> torch.Tensor:
     FP8 cache whose elements are code values times ``scale``."""
     x = normal_tensor(rng, shape, "bf16").float() / scale
     return x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def fp8_codes_device(gen: torch.Generator, shape, scale: float, device,
+                     chunk_elems: int = 1 << 26) -> torch.Tensor:
+    """The same as ``fp8_codes`` from a seeded device generator, made on the
+    device."""
+    out = torch.empty(tuple(shape), dtype=torch.uint8, device=device)
+    flat = out.view(-1)
+    for s in range(0, flat.numel(), chunk_elems):
+        e = min(flat.numel(), s + chunk_elems)
+        x = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32)
+        x = x.to(torch.bfloat16).float() / scale
+        flat[s:e] = x.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
 
 
 @dataclass

@@ -1,23 +1,30 @@
 """pa_decode_static_workspace: the split decode whose partition workspace is
 a fixed buffer inside the library, for callers that cannot allocate device
 memory (a host framework owns the pool, or cudaMalloc's synchronisation is
-not acceptable).  Its output must match the caller-workspace path
-(pa_decode_split + pa_reduce) within the parity tolerance, call after call,
-although every call reuses the same buffer.
+not acceptable).
+
+It runs the same kernels on the same partitions as pa_decode_split +
+pa_reduce with a caller-owned workspace, so its output must equal that path
+bit for bit, call after call, although every call reuses the same buffer;
+and it must match the CPU reference within the parity tolerance.
 
 This file is named to run last, so that a failure here comes after every
 other test has run; it also passes on its own in a fresh process.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_226_gb300 import build, lib
 from paged_kv_cache_226_gb300 import inputs as pin
 from parity_util import assert_close, to_device
 
 pytestmark = pytest.mark.gpu
+
+LIMIT = 32 << 20          # PA_STATIC_WORKSPACE_BYTES
 
 
 @pytest.fixture(scope="module")
@@ -29,26 +36,52 @@ def dev():
     return torch.device("cuda:0")
 
 
-def _via_c_abi(w, d, partition):
-    """Call the static-workspace entry point directly through ctypes."""
+def _static_call(w, d, partition, S, out=None, partition_arg=None):
+    """The static-workspace entry point called directly through ctypes;
+    returns (status, out)."""
     pa = lib.load()
-    out = torch.empty_like(d["q"])
+    out = torch.empty_like(d["q"]) if out is None else out
     shp = lib.make_shape(w.num_seqs, w.num_q_heads, d["k_cache"], w.max_blocks_per_seq)
-    S = lib.num_partitions(int(w.context_lens.max()), partition)
     st = pa.pa_decode_static_workspace(
         ctypes.c_void_p(d["q"].data_ptr()), ctypes.c_void_p(d["k_cache"].data_ptr()),
         ctypes.c_void_p(d["v_cache"].data_ptr()), ctypes.c_void_p(d["block_tables"].data_ptr()),
         ctypes.c_void_p(d["context_lens"].data_ptr()), ctypes.c_float(w.scale),
-        partition, S, ctypes.c_void_p(out.data_ptr()), ctypes.byref(shp),
+        partition if partition_arg is None else partition_arg, S,
+        ctypes.c_void_p(out.data_ptr()), ctypes.byref(shp),
         ctypes.c_void_p(torch.cuda.current_stream(d["q"].device).cuda_stream))
-    assert st == lib.PA_OK, lib.status_string(st)
+    return st, out
+
+
+def _caller_workspace(w, d, partition, S):
+    """pa_decode_split + pa_reduce with a workspace the caller allocates."""
+    tmp, ml, es = lib.decode_split(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                   d["context_lens"], w.scale, partition, S)
+    out = torch.empty_like(d["q"])
+    lib.reduce(tmp, ml, es, d["context_lens"], partition, d["k_cache"], w.max_blocks_per_seq,
+               out)
     return out
 
 
-def _via_caller_workspace(w, d, partition):
-    return lib.paged_attention(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
-                               d["context_lens"], w.scale, int(w.context_lens.max()),
-                               mode="split", partition_size=partition)
+def _bits(t):
+    return pin.bits(t.cpu())
+
+
+def _oracle(w):
+    return oracle.paged_decode(pin.bits(w.q), pin.bits(w.k_cache), pin.bits(w.v_cache),
+                               w.block_tables, w.context_lens, w.scale, w.dtype)
+
+
+def _max_partitions_that_fit(B, hq, d):
+    """Largest S whose workspace -- [tmp_out][max_logits][exp_sums], each
+    part rounded up to 256 bytes -- fits in the buffer."""
+    def need(S):
+        rows = B * hq * S
+        r256 = lambda x: (x + 255) // 256 * 256
+        return r256(4 * rows * d) + 2 * r256(4 * rows)
+    S = 1
+    while need(S + 1) <= LIMIT:
+        S += 1
+    return S, need(S), need(S + 1)
 
 
 def test_static_workspace_matches_caller_workspace_twice(dev):
@@ -61,25 +94,56 @@ def test_static_workspace_matches_caller_workspace_twice(dev):
                                  seed=77), 64)]
     for w, P in cases:
         d = to_device(w, dev)
-        want = _via_caller_workspace(w, d, P).float().cpu().numpy()
-        got = _via_c_abi(w, d, P).float().cpu().numpy()
-        assert_close(got, want, f"static workspace vs caller workspace ({w.name})")
+        S = lib.num_partitions(int(w.context_lens.max()), P)
+        want = _caller_workspace(w, d, P, S)
+        st, got = _static_call(w, d, P, S)
+        assert st == lib.PA_OK, lib.status_string(st)
+        assert np.array_equal(_bits(got), _bits(want)), \
+            f"static workspace differs from the caller-workspace path ({w.name})"
+        # the second call through the Python binding of the same entry point
         again = lib.decode_static_workspace(d["q"], d["k_cache"], d["v_cache"],
                                             d["block_tables"], d["context_lens"], w.scale,
                                             int(w.context_lens.max()), partition_size=P)
-        assert_close(again.float().cpu().numpy(), want, f"second call ({w.name})")
+        assert np.array_equal(_bits(again), _bits(want)), f"second call differs ({w.name})"
+        assert_close(again.float().cpu().numpy(), _oracle(w), f"static workspace vs oracle "
+                                                               f"({w.name})")
     assert lib.read_device_errors(dev) == 0
 
 
-def test_static_workspace_rejects_requests_over_its_limit(dev):
+def test_static_workspace_limit_edge(dev):
+    """A request that fills the buffer exactly as far as the rounding rule
+    allows runs and matches the caller-workspace path; one more partition is
+    refused with PA_ERR_WORKSPACE."""
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=1, lens=[1000], num_q_heads=8,
+                                       num_kv_heads=2, head_dim=128, block_size=16), seed=31)
+    S, need, need_next = _max_partitions_that_fit(1, 8, 128)
+    assert need <= LIMIT < need_next
+    d = to_device(w, dev)
+    P = 16                                  # 63 live partitions, the rest past the end
+    want = _caller_workspace(w, d, P, S)
+    st, got = _static_call(w, d, P, S)
+    assert st == lib.PA_OK, lib.status_string(st)
+    assert np.array_equal(_bits(got), _bits(want))
+    assert_close(got.float().cpu().numpy(), _oracle(w), "static workspace at its limit")
+    sentinel = torch.full_like(d["q"], 7.0)
+    st, after = _static_call(w, d, P, S + 1, out=sentinel)
+    assert st == lib.PA_ERR_WORKSPACE
+    torch.cuda.synchronize(dev)
+    assert bool((after == 7.0).all()), "a refused request wrote its output"
+    assert lib.read_device_errors(dev) == 0
+
+
+def test_static_workspace_error_order(dev):
+    """Malformed requests get the status pa_decode_split + pa_reduce give
+    them, before the size limit is considered."""
     w = pin.build_workload("tiny")
     d = to_device(w, dev)
-    pa = lib.load()
-    shp = lib.make_shape(w.num_seqs, w.num_q_heads, d["k_cache"], w.max_blocks_per_seq)
-    # 4 seqs x 8 heads x S x 64 dims x 4 B > 32 MiB once S > 4096
-    st = pa.pa_decode_static_workspace(
-        ctypes.c_void_p(d["q"].data_ptr()), ctypes.c_void_p(d["k_cache"].data_ptr()),
-        ctypes.c_void_p(d["v_cache"].data_ptr()), ctypes.c_void_p(d["block_tables"].data_ptr()),
-        ctypes.c_void_p(d["context_lens"].data_ptr()), ctypes.c_float(w.scale), 16, 5000,
-        ctypes.c_void_p(d["q"].data_ptr()), ctypes.byref(shp), None)
+    # 4 seqs x 8 heads x 5000 partitions x 64 dims x 4 B is far over 32 MiB
+    st, _ = _static_call(w, d, 16, 5000)
+    assert st == lib.PA_ERR_WORKSPACE
+    st, _ = _static_call(w, d, 16, 5000, partition_arg=24)      # not a multiple of the block
+    assert st == lib.PA_ERR_INVALID_ARG
+    st, _ = _static_call(w, d, 16, 70000)                        # over 65535 partitions
+    assert st == lib.PA_ERR_UNSUPPORTED
+    st, _ = _static_call(w, d, 16, 0)
     assert st == lib.PA_ERR_WORKSPACE
