@@ -461,6 +461,7 @@ SUB_CONFIGS = {
     "llama8b_split512": ("llama8b", "split", 512, "auto"),
     "llama8b_fp8": ("llama8b", "fused", 0, "fp8"),
     "prefix": ("prefix", "fused", 0, "auto"),
+    "prefix_balanced": ("prefix", "balanced", 0, "auto"),
     "llama70b": ("llama70b", "fused", 0, "auto"),
     "long16": ("long16", "fused", 0, "auto"),
     "long16_split512": ("long16", "split", 512, "auto"),

@@ -161,16 +161,17 @@ int pa_reduce(const float* tmp_out, const float* max_logits, const float* exp_su
  * inputs, same results) with the work balanced over one wave of CTAs instead
  * of one CTA per context partition: the 16-token tiles of all (sequence,
  * KV head) pairs, in order, are dealt out in equal contiguous ranges to the
- * consumer warps of the grid; a warp's range may cover the end of one
- * sequence and the start of the next, and pieces of one (sequence, KV head)
- * are merged (log-sum-exp) by the warp that finishes last.  Suited to
- * batches of many short or ragged contexts.
+ * consumer warps of the grid, each CTA's TMA producer warp serving its two
+ * consumers; a warp's range may cover the end of one sequence and the start
+ * of the next, and pieces of one (sequence, KV head) are merged
+ * (log-sum-exp) by the warp that finishes last.  Suited to batches of many
+ * short or ragged contexts.
  * workspace: device memory of at least pa_balanced_workspace_size(shp)
  * bytes, 16-byte aligned, all zero before the first call (it holds
  * per-(sequence, KV head) counters that every call leaves at zero; zero it
  * again after a PA_DEVERR_WAIT_TIMEOUT).  Calls that overlap on the GPU must
  * not share a workspace.  Other arguments and errors as pa_decode_step.
- * Two launches (a one-CTA plan kernel, then the attention kernel).
+ * One launch.
  */
 size_t pa_balanced_workspace_size(const pa_shape* shp);
 int pa_decode_step_balanced(const void* q, const void* k, const void* v,

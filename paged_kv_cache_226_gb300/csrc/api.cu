@@ -155,6 +155,13 @@ int check_decode_args(const void* q, const void* k_cache, const void* v_cache,
     return PA_OK;
 }
 
+#ifdef PA_TEST_HOOKS
+// Test builds only: the wait fault of pa_test_set_wait_fault (none by default).
+int g_test_cta = -1;
+int g_test_tile = 0;
+unsigned long long g_test_wait_limit_ns = pa::kWaitLimitNs;
+#endif
+
 pa::DecodeParams make_params(const void* q, const int32_t* block_tables,
                              const int32_t* context_lens, float scale, const pa_shape* shp,
                              int* err, const CacheKind& ck) {
@@ -172,6 +179,11 @@ pa::DecodeParams make_params(const void* q, const int32_t* block_tables,
     p.block_size = shp->block_size;
     p.num_blocks = shp->num_blocks;
     p.num_kv_heads = shp->num_kv_heads;
+#ifdef PA_TEST_HOOKS
+    p.test_cta = g_test_cta;
+    p.test_tile = g_test_tile;
+    p.test_wait_limit_ns = g_test_wait_limit_ns;
+#endif
     return p;
 }
 
@@ -229,6 +241,16 @@ const char* pa_status_string(int status) {
 }
 
 int pa_last_cuda_error(void) { return t_last_cuda_error; }
+
+#ifdef PA_TEST_HOOKS
+int pa_test_set_wait_fault(int32_t cta, int32_t tile, unsigned long long wait_limit_ns) {
+    if (wait_limit_ns == 0) return PA_ERR_INVALID_ARG;
+    g_test_cta = cta;
+    g_test_tile = tile;
+    g_test_wait_limit_ns = wait_limit_ns;
+    return PA_OK;
+}
+#endif
 
 int pa_read_device_errors(int32_t* flags, void* stream) {
     if (flags == nullptr) return PA_ERR_INVALID_ARG;
@@ -386,29 +408,37 @@ int decode_step(const void* q, const void* k, const void* v, const int64_t* slot
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
-// Consumer warps of the balanced step's grid on the current device (one wave:
-// every SM holds the 16-bit kernel's resident CTAs; the FP8 grid uses fewer).
+// CTAs of the balanced step's grid on the current device: one wave, every SM
+// holding the decode kernel's resident CTAs.
 cudaError_t balanced_grid(int* num_ctas, bool fp8) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    (void)fp8;
-    *num_ctas = sms * pa::kStreamCtasPerSm;
+    *num_ctas = sms * (fp8 ? pa::kMinCtasPerSmFp8 : pa::kMinCtasPerSm);
+    return cudaSuccess;
+}
+
+// Consumer warps of the larger of the two grids (16-bit and FP8 caches).
+cudaError_t balanced_max_warps(int* warps) {
+    int a = 0, b = 0;
+    cudaError_t e = balanced_grid(&a, false);
+    if (e == cudaSuccess) e = balanced_grid(&b, true);
+    if (e != cudaSuccess) return e;
+    *warps = (a > b ? a : b) * pa::kConsumerWarps;
     return cudaSuccess;
 }
 
 struct BalancedWorkspace {
     int* counters;
-    int* plan;
     float* rec_m;
     float* rec_l;
     float* rec_o;
     size_t bytes;
 };
 
-// [counters B*Hkv][plan][rec_m R*G][rec_l R*G][rec_o R*G*D], each part
-// 256-byte aligned, R = max consumer warps + B*Hkv.
+// [counters B*Hkv][rec_m R*G][rec_l R*G][rec_o R*G*D], each part 256-byte
+// aligned, R = max consumer warps + B*Hkv.
 BalancedWorkspace balanced_layout(const pa_shape* s, int max_warps, void* base) {
     const size_t B = s->num_seqs, Hkv = s->num_kv_heads, G = s->num_q_heads / s->num_kv_heads;
     const size_t R = (size_t)max_warps + B * Hkv;
@@ -420,8 +450,6 @@ BalancedWorkspace balanced_layout(const pa_shape* s, int max_warps, void* base) 
         return static_cast<unsigned char*>(base) + at;
     };
     w.counters = reinterpret_cast<int*>(take(B * Hkv * sizeof(int)));
-    w.plan = reinterpret_cast<int*>(
-        take(((size_t)pa::plan_starts_offset((int)B) + 4 * (size_t)max_warps) * sizeof(int)));
     w.rec_m = reinterpret_cast<float*>(take(R * G * sizeof(float)));
     w.rec_l = reinterpret_cast<float*>(take(R * G * sizeof(float)));
     w.rec_o = reinterpret_cast<float*>(take(R * G * s->head_dim * sizeof(float)));
@@ -445,11 +473,11 @@ int decode_step_balanced(const void* q, const void* k, const void* v, const int6
             (shp->block_size / pa::kTileTokens) >= (1ll << 31))
         return PA_ERR_UNSUPPORTED;
     if (!workspace || !aligned16(workspace)) return PA_ERR_WORKSPACE;
-    int num_ctas = 0, max_ctas = 0;
+    int num_ctas = 0, max_warps = 0;
     cudaError_t e = balanced_grid(&num_ctas, ck.fp8);
-    if (e == cudaSuccess) e = balanced_grid(&max_ctas, false);
+    if (e == cudaSuccess) e = balanced_max_warps(&max_warps);
     if (e != cudaSuccess) return cuda_fail(e);
-    BalancedWorkspace w = balanced_layout(shp, max_ctas * pa::kStreamWarps, workspace);
+    BalancedWorkspace w = balanced_layout(shp, max_warps, workspace);
     if (w.bytes > workspace_bytes) return PA_ERR_WORKSPACE;
     CUtensorMap tmk, tmv;
     if ((st = encode_cache_map(&tmk, k_cache, shp, ck.fp8)) != PA_OK) return st;
@@ -479,8 +507,7 @@ int decode_step_balanced(const void* q, const void* k, const void* v, const int6
     p.k_scale = ck.k_scale;
     p.v_scale = ck.v_scale;
     p.num_seqs = shp->num_seqs;
-    p.num_warps = num_ctas * pa::kStreamWarps;
-    p.plan = w.plan;
+    p.num_warps = num_ctas * pa::kConsumerWarps;
     p.rec_o = w.rec_o;
     p.rec_m = w.rec_m;
     p.rec_l = w.rec_l;
@@ -565,9 +592,9 @@ extern "C" {
 
 size_t pa_balanced_workspace_size(const pa_shape* shp) {
     if (check_shape(shp, true) != PA_OK) return 0;
-    int max_ctas = 0;
-    if (balanced_grid(&max_ctas, false) != cudaSuccess) return 0;
-    return balanced_layout(shp, max_ctas * pa::kStreamWarps, nullptr).bytes;
+    int max_warps = 0;
+    if (balanced_max_warps(&max_warps) != cudaSuccess) return 0;
+    return balanced_layout(shp, max_warps, nullptr).bytes;
 }
 
 int pa_decode_step_balanced(const void* q, const void* k, const void* v,

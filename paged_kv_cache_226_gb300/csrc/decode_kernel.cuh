@@ -83,6 +83,13 @@ __device__ __forceinline__ uint4 new_token_chunk(const DecodeParams& p, int b, i
     return make_uint4(codes.x, codes.y, 0u, 0u);
 }
 
+// The wait limit of the pipeline barriers (a test build can shorten it).
+#ifdef PA_TEST_HOOKS
+#define PA_DECODE_WAIT_LIMIT(p) ((p).test_wait_limit_ns)
+#else
+#define PA_DECODE_WAIT_LIMIT(p) kWaitLimitNs
+#endif
+
 template <typename T, int D, int kMode, bool kFp8 = false>
 __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMinCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -164,21 +171,28 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         }
         const int32_t* table = p.block_tables + (size_t)b * p.max_blocks_per_seq;
         const int tiles_per_block = p.block_size / kTileTokens;
+        int issue_end = n_tiles;                        // tiles this producer issues
+#ifdef PA_TEST_HOOKS
+        if ((long long)blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y *
+                                                            blockIdx.z) == p.test_cta)
+            issue_end = min(n_tiles, max(0, p.test_tile));
+#endif
         bool ok = true;
-        for (int i0 = 0; i0 < n_tiles && ok; i0 += 32) {
+        for (int i0 = 0; i0 < issue_end && ok; i0 += 32) {
             const int mine = i0 + lane;
             int blk = 0;
             if (mine < n_tiles) {
                 blk = __ldg(table + (tile_begin + mine) / tiles_per_block);
                 if (blk < 0 || blk >= p.num_blocks) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
             }
-            const int cnt = min(32, n_tiles - i0);
+            const int cnt = min(32, issue_end - i0);
             for (int k = 0; k < cnt; ++k) {
                 const int pblk = __shfl_sync(0xffffffffu, blk, k);
                 if (lane == 0) {
                     const int it = i0 + k;
                     const int st = it % Lay::kRing;
-                    if (it >= Lay::kRing && !mbar_wait(&empty_bar[st], ((it / Lay::kRing) - 1) & 1)) {
+                    if (it >= Lay::kRing && !mbar_wait(&empty_bar[st], ((it / Lay::kRing) - 1) & 1,
+                                                       PA_DECODE_WAIT_LIMIT(p))) {
                         flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
                         ok = false;
                     } else {
@@ -253,7 +267,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
 
     for (int it = warp; it < n_tiles; it += kConsumerWarps) {
         const int st = it % Lay::kRing;
-        bool ok = mbar_wait(&full_bar[st], (it / Lay::kRing) & 1);
+        bool ok = mbar_wait(&full_bar[st], (it / Lay::kRing) & 1, PA_DECODE_WAIT_LIMIT(p));
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
             break;
@@ -272,10 +286,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
                 __syncwarp();
             }
             attend_tile_fp8(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
-                            scale_log2, lane, [&] {
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(&empty_bar[st]);
-                            });
+                            scale_log2, lane, [&] { release_stage(&empty_bar[st], lane); });
         } else {
             if (kMode == kModeStep && it == new_tile) {
                 // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V
@@ -290,8 +301,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
             }
             attend_tile<T, D>(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
                               scale_log2, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[st]);
+            release_stage(&empty_bar[st], lane);
         }
     }
 

@@ -41,22 +41,9 @@ static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of consu
 constexpr int kStagesFp8 = PA_DECODE_STAGES_FP8;
 constexpr int kMinCtasPerSmFp8 = PA_DECODE_MIN_CTAS_PER_SM_FP8;
 static_assert(kStagesFp8 % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
-// Work-balanced step (balanced.cu): every warp of a CTA streams its own tile
-// range and issues its own TMA loads into a private ring of
-// PA_STREAM_RING_KIB KiB (16-bit tiles; an FP8 warp keeps 8 KiB of it for its
-// 16-bit copy of the tile).
-#ifndef PA_STREAM_WARPS
-#define PA_STREAM_WARPS 4
-#endif
-#ifndef PA_STREAM_RING_KIB
-#define PA_STREAM_RING_KIB 24
-#endif
-#ifndef PA_STREAM_CTAS_PER_SM
-#define PA_STREAM_CTAS_PER_SM 2
-#endif
-constexpr int kStreamWarps = PA_STREAM_WARPS;
-constexpr int kStreamRingBytes = PA_STREAM_RING_KIB * 1024;
-constexpr int kStreamCtasPerSm = PA_STREAM_CTAS_PER_SM;
+// A wait on a pipeline barrier gives up after this many nanoseconds and
+// reports PA_DEVERR_WAIT_TIMEOUT instead of spinning forever.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kMaxGroup = 8;         // query heads per KV head served by one CTA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -89,9 +76,20 @@ struct DecodeParams {
     // FP8 (E4M3) cache only: per-tensor scales (k_scale is also folded into scale_log2)
     float k_scale;
     float v_scale;
+#ifdef PA_TEST_HOOKS
+    // Test builds only (libpa_test.so): the producer of CTA test_cta (linear
+    // index, -1: none) issues no tile from test_tile on, and every pipeline
+    // wait gives up after test_wait_limit_ns, so a test can make the
+    // consumers' bounded waits run out without a copy in flight.
+    int test_cta;
+    int test_tile;
+    unsigned long long test_wait_limit_ns;
+#endif
 };
 
-// Work-balanced fused step (balanced.cu).
+// Work-balanced fused step (balanced.cu): one wave of the fused step's CTAs,
+// every consumer warp streaming an equal contiguous range of the (sequence,
+// KV head, tile) order.
 struct BalancedParams {
     const void* q;
     const int32_t* block_tables;
@@ -109,21 +107,16 @@ struct BalancedParams {
     const int64_t* slot_mapping;
     void* k_cache;
     void* v_cache;
-    int* counters;                 // [B][Hkv], 0 on entry and on exit
+    int* counters;                 // [B][Hkv] pieces finished, 0 on entry and on exit
     int num_kv_heads;
     float k_scale;
     float v_scale;
     int num_seqs;
     int num_warps;                 // consumer warps of the grid
-    int* plan;                     // [N, Q, prefix[B + 1]]
     float* rec_o;                  // [R][G][D] partial outputs, R = num_warps + B * Hkv
     float* rec_m;                  // [R][G]
     float* rec_l;                  // [R][G]
 };
-
-// Layout of the balanced step's plan (ints): [N, Q, prefix[B + 1], pad,
-// start cursors int4[num_warps] from this offset on (16-byte aligned).
-__host__ __device__ __forceinline__ int plan_starts_offset(int B) { return ((B + 3 + 3) / 4) * 4; }
 
 cudaError_t launch_balanced(int dtype, int head_dim, bool fp8, const CUtensorMap& tmk,
                             const CUtensorMap& tmv, const BalancedParams& p, int num_ctas,

@@ -267,8 +267,7 @@ __global__ void __launch_bounds__((kMaxGroup + 1) * 32)
                 M::run(o[2 * np + 1], pl0, pl1, pl2, pl3, b2, b3);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[st]);
+        release_stage(&empty_bar[st], lane);
     }
 
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);

@@ -20,6 +20,12 @@ def test_exports_every_header_symbol(pa):
         assert hasattr(pa, n), f"libpa.so does not export {n}"
 
 
+def test_product_library_has_no_test_hook(pa):
+    """The failure-detection hook (include/pa_test.h) exists only in the test
+    build, libpa_test.so."""
+    assert not hasattr(pa, "pa_test_set_wait_fault")
+
+
 def test_status_strings(pa):
     assert lib.status_string(lib.PA_OK) == "ok"
     assert "unsupported" in lib.status_string(lib.PA_ERR_UNSUPPORTED)

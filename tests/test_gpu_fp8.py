@@ -133,3 +133,33 @@ def test_fp8_rejects_head_dim_64_and_bad_scales(dev):
     kc2 = torch.zeros((4, 16, 2, 128), dtype=torch.uint8, device=dev)
     with pytest.raises(lib.PaError, match="invalid"):
         lib.decode_fp8(q2, kc2, kc2, bt, cl, 0.1, 0.0, 1.0)
+
+
+@pytest.mark.parametrize("mode", ["fused", "balanced"])
+def test_fp8_repeated_steps(dev, mode):
+    """Eight layer-steps over fresh copies of the same cache, each against the
+    reference.  An FP8 tile hands its ring stage back before its P.V products;
+    before the stage release ordered the warp's reads ahead of the refill
+    (a proxy fence), about half of such runs had one partition of one
+    (sequence, KV head) computed from a half-overwritten tile."""
+    w, kc, vc = _fp8_case("llama70b")
+    d = {k: (torch.from_numpy(v) if isinstance(v, np.ndarray) else v).to(dev)
+         for k, v in dict(q=w.q, k_new=w.k_new, v_new=w.v_new, bt=w.block_tables,
+                          cl=w.context_lens, sm=w.slot_mapping).items()}
+    wk, wv, _ = oracle.reshape_and_cache_fp8(pin.bits(w.k_new), pin.bits(w.v_new),
+                                             w.slot_mapping, kc.numpy(), vc.numpy(),
+                                             w.block_size, w.dtype, K_SCALE, V_SCALE)
+    want = oracle.paged_decode_fp8(pin.bits(w.q), wk, wv, w.block_tables, w.context_lens,
+                                   w.scale, K_SCALE, V_SCALE, w.dtype)
+    max_len = int(w.context_lens.max())
+    for trial in range(8):
+        kd, vd = kc.to(dev), vc.to(dev)
+        if mode == "fused":
+            out = lib.decode_step_fp8(d["q"], d["k_new"], d["v_new"], d["sm"], kd, vd, d["bt"],
+                                      d["cl"], w.scale, K_SCALE, V_SCALE, max_len)
+        else:
+            out = lib.decode_step_balanced(d["q"], d["k_new"], d["v_new"], d["sm"], kd, vd,
+                                           d["bt"], d["cl"], w.scale, k_scale=K_SCALE,
+                                           v_scale=V_SCALE)
+        assert_close(out.float().cpu().numpy(), want, f"{mode} fp8 step, run {trial}")
+    assert lib.read_device_errors(dev) == 0
