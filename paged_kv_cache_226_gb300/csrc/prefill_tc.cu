@@ -42,6 +42,11 @@
 
 namespace pa {
 
+// bf16 P as a hi + lo pair (two P V products) or rounded once to bf16
+#ifndef PA_PREFILL_SPLIT_P
+#define PA_PREFILL_SPLIT_P 1
+#endif
+
 constexpr int kTcRows = 128;                 // query rows per CTA (tokens x heads)
 constexpr int kTcKeys = 128;                 // keys per K/V tile
 constexpr int kTcKStages = 3;                // K tiles in flight (free once S is computed)
@@ -85,7 +90,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const __grid_constant__ CUtensorMap tmap_v,
                             const __grid_constant__ PrefillParams p) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    constexpr bool kSplitP = kBf16;
+    constexpr bool kSplitP = kBf16 && PA_PREFILL_SPLIT_P;
     using Lay = TcLayout;
     using M = Mma<T>;
     __shared__ __align__(8) uint64_t k_full[kTcKStages], k_empty[kTcKStages];
