@@ -87,3 +87,20 @@ def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     (prof / "paged_prefill_w.json").write_text(json.dumps(rec))
     assert bench.profiled_traffic("w", "paged_prefill") is None
     assert bench.profiled_traffic("absent", "paged_prefill") is None
+
+
+def test_choose_partition_rule():
+    """The partition size rule on a 152-SM part with six decode CTAs per SM
+    (912 slots): many (sequence, KV head) pairs get 1024-token partitions,
+    few pairs about one partition per slot (a multiple of 512, at most 4096),
+    short contexts 512."""
+    from paged_kv_cache_226_gb300 import lib
+    if __import__("torch").cuda.is_available():
+        pytest.skip("the rule is checked here for the 152-SM default only")
+    assert lib.choose_partition(64, 8, 2048) == 1024            # 512 pairs
+    assert lib.choose_partition(256, 8, 4608) == 1024           # shared-prefix batch
+    assert lib.choose_partition(32, 8, 4096) == 1536            # 256 pairs: ceil(1150 / 512)
+    assert lib.choose_partition(8, 8, 50000) == 3584            # 64 pairs: ceil(3509 / 512)
+    assert lib.choose_partition(1, 1, 10 ** 6) == 4096          # clamped
+    assert lib.choose_partition(4, 2, 250) == 512               # short contexts
+    assert lib.choose_partition(64, 8, 2048, block_size=32) % 32 == 0
