@@ -101,6 +101,7 @@ def test_choose_partition_rule():
     assert lib.choose_partition(256, 8, 4608) == 1024           # shared-prefix batch
     assert lib.choose_partition(32, 8, 4096) == 1536            # 256 pairs: ceil(1150 / 512)
     assert lib.choose_partition(8, 8, 50000) == 3584            # 64 pairs: ceil(3509 / 512)
-    assert lib.choose_partition(1, 1, 10 ** 6) == 4096          # clamped
+    assert lib.choose_partition(1, 1, 10 ** 6) == 1536          # ceil(1097 / 512)
+    assert lib.choose_partition(1, 1, 10 ** 7) == 4096          # clamped
     assert lib.choose_partition(4, 2, 250) == 512               # short contexts
     assert lib.choose_partition(64, 8, 2048, block_size=32) % 32 == 0
