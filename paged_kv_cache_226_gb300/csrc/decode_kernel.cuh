@@ -177,40 +177,61 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
                                                             blockIdx.z) == p.test_cta)
             issue_end = min(n_tiles, max(0, p.test_tile));
 #endif
+        // Tiles go out in rounds of kBatch: in a round, lane t * kBoxes + j
+        // issues box j (K halves, then V halves) of tile i + t after waiting
+        // itself for that tile's stage, so one warp instruction issues every
+        // box of the round.  With one issuing lane the stage wait, the byte
+        // count and each copy are paid in sequence, ~600-750 cycles a tile,
+        // which is what held a CTA streaming alone over an FP8 cache to
+        // 12 GB/s (17 GB/s in rounds of two).  Lane l holds the table
+        // entries of tiles i0 + l (blk) and i0 + 32 + l (blk_next, read a
+        // chunk ahead so a new chunk does not wait for the table).
+        constexpr int kBoxes = 2 * Lay::kHalves;
+        constexpr int kBatch = kIssueBatch < Lay::kRing ? kIssueBatch : Lay::kRing;
+        static_assert(kBatch * kBoxes <= 32 && 32 % kBatch == 0, "a round fits one warp");
+        const int t_lane = lane / kBoxes, box = lane % kBoxes;
+        const int hh = box % Lay::kHalves;
+        const bool is_v = box >= Lay::kHalves;
+        const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
+        auto entry = [&](int tile) {
+            int e = 0;
+            if (tile < n_tiles) {
+                e = __ldg(table + (tile_begin + tile) / tiles_per_block);
+                if (e < 0 || e >= p.num_blocks) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+            }
+            return e;
+        };
+        int blk = entry(lane);
+        int blk_next = entry(32 + lane);
         bool ok = true;
         for (int i0 = 0; i0 < issue_end && ok; i0 += 32) {
-            const int mine = i0 + lane;
-            int blk = 0;
-            if (mine < n_tiles) {
-                blk = __ldg(table + (tile_begin + mine) / tiles_per_block);
-                if (blk < 0 || blk >= p.num_blocks) flag_error(p.err, PA_DEVERR_BAD_CONTEXT);
+            if (i0 > 0) {
+                blk = blk_next;
+                blk_next = entry(i0 + 32 + lane);
             }
             const int cnt = min(32, issue_end - i0);
-            for (int k = 0; k < cnt; ++k) {
-                const int pblk = __shfl_sync(0xffffffffu, blk, k);
-                if (lane == 0) {
-                    const int it = i0 + k;
-                    const int st = it % Lay::kRing;
-                    if (it >= Lay::kRing && !mbar_wait(&empty_bar[st], ((it / Lay::kRing) - 1) & 1,
-                                                       PA_DECODE_WAIT_LIMIT(p))) {
-                        flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
-                        ok = false;
-                    } else {
-                        mbar_arrive_expect_tx(&full_bar[st], Lay::kStageBytes);
-                        const int sub = ((tile_begin + it) % tiles_per_block) * kTileTokens;
-                        uint8_t* kdst = smem + st * Lay::kStageBytes;
-                        uint8_t* vdst = kdst + Lay::kTileBytes;
-#pragma unroll
-                        for (int hh = 0; hh < Lay::kHalves; ++hh) {
-                            tma_load_4d(kdst + hh * Lay::kBoxBytes, &tmap_k, &full_bar[st],
-                                        hh * kBoxElems, g, sub, pblk);
-                            tma_load_4d(vdst + hh * Lay::kBoxBytes, &tmap_v, &full_bar[st],
-                                        hh * kBoxElems, g, sub, pblk);
-                        }
-                    }
+            for (int k = 0; k < cnt; k += kBatch) {
+                const int pblk = __shfl_sync(0xffffffffu, blk, (k + t_lane) & 31);
+                const int it = i0 + k + t_lane;
+                const bool act = t_lane < kBatch && k + t_lane < cnt;
+                const int st = it % Lay::kRing;
+                bool good = true;
+                if (act && it >= Lay::kRing)
+                    good = mbar_wait(&empty_bar[st], ((it / Lay::kRing) - 1) & 1,
+                                     PA_DECODE_WAIT_LIMIT(p));
+                if (act && good && box == 0) mbar_arrive_expect_tx(&full_bar[st], Lay::kStageBytes);
+                // the vote also puts every expect_tx of the round before its copies
+                if (!__all_sync(0xffffffffu, good)) {
+                    if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                if (act) {
+                    const int sub = ((tile_begin + it) % tiles_per_block) * kTileTokens;
+                    uint8_t* dst = smem + st * Lay::kStageBytes + (is_v ? Lay::kTileBytes : 0) +
+                                   hh * Lay::kBoxBytes;
+                    tma_load_4d(dst, tmap, &full_bar[st], hh * kBoxElems, g, sub, pblk);
+                }
             }
         }
         return;

@@ -41,6 +41,13 @@ static_assert(kStages % kConsumerWarps == 0, "stages must be a multiple of consu
 constexpr int kStagesFp8 = PA_DECODE_STAGES_FP8;
 constexpr int kMinCtasPerSmFp8 = PA_DECODE_MIN_CTAS_PER_SM_FP8;
 static_assert(kStagesFp8 % kConsumerWarps == 0, "stages must be a multiple of consumer warps");
+// Tiles the decode producer issues per round (one lane per TMA box); two
+// measured best: four delays the first copies of a round behind the last
+// stage it waits for (shared-prefix batch 148 against 132 us).
+#ifndef PA_DECODE_ISSUE_BATCH
+#define PA_DECODE_ISSUE_BATCH 2
+#endif
+constexpr int kIssueBatch = PA_DECODE_ISSUE_BATCH;
 // A wait on a pipeline barrier gives up after this many nanoseconds and
 // reports PA_DEVERR_WAIT_TIMEOUT instead of spinning forever.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
