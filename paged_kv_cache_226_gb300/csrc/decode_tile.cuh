@@ -91,8 +91,15 @@ __device__ __forceinline__ void fp8_dims(int n, int r8, int& d_lo, int& d_hi) {
     d_hi = d_lo + 1;
 }
 
+// 16-byte shared-memory load.  The tile pointers come from an aligned
+// integer offset of the dynamic shared buffer, so a plain dereference would
+// compile to a generic load; this one is a shared load.
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
-    return *reinterpret_cast<const uint4*>(p);
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
