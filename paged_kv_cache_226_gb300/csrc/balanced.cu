@@ -493,10 +493,12 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         }
         if constexpr (kFp8) {
             // the codes are in registers: the stage can be refilled
-            attend_tile_fp8(ts, qb, ktile, vtile, t * kTileTokens, L, scale_log2, lane,
+            attend_tile_fp8(ts, [&](int kk, uint32_t& b0, uint32_t& b1) { b0 = qb[kk][0]; b1 = qb[kk][1]; },
+                            ktile, vtile, t * kTileTokens, L, scale_log2, lane,
                             [&] { release_stage(&empty_bar[st], lane); });
         } else {
-            attend_tile<T, D>(ts, qb, ktile, vtile, t * kTileTokens, L, scale_log2, lane);
+            attend_tile<T, D>(ts, [&](int kk, uint32_t& b0, uint32_t& b1) { b0 = qb[kk][0]; b1 = qb[kk][1]; },
+                              ktile, vtile, t * kTileTokens, L, scale_log2, lane);
             release_stage(&empty_bar[st], lane);
         }
 
@@ -586,7 +588,8 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
 template <typename T, int D, bool kFp8>
 cudaError_t launch_balanced_t(const CUtensorMap& tmk, const CUtensorMap& tmv,
                               const BalancedParams& p, int num_ctas, cudaStream_t stream) {
-    const int smem = DecodeLayout<D, kFp8>::kDynamicSmem;
+    // this kernel holds its q fragments in registers: no q area
+    const int smem = DecodeLayout<D, kFp8>::kDynamicSmem - DecodeLayout<D, kFp8>::kQBytes;
     cudaError_t e = cudaFuncSetAttribute(balanced_step_kernel<T, D, kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

@@ -48,7 +48,10 @@ struct DecodeLayout {
     static constexpr int kMergeBytes = kConsumerWarps * kMergeFloatsPerWarp * 4;
     static constexpr int kBodyBytes = (kPipeBytes + kConvBytes) > kMergeBytes
                                           ? (kPipeBytes + kConvBytes) : kMergeBytes;
-    static constexpr int kDynamicSmem = kBodyBytes + 1024;         // + alignment slack
+    // q^T fragments of the group, [D/16 k-steps][32 lanes][2 words], read
+    // per k-step instead of held in 16 registers through the tile loop
+    static constexpr int kQBytes = (D / 16) * 32 * 8;
+    static constexpr int kDynamicSmem = kBodyBytes + kQBytes + 1024;  // + alignment slack
 };
 
 // The fused step's new token, 16-byte chunk c (8 dims) of its K (is_k) or V
@@ -262,6 +265,19 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
             load_q_fragments<T, D>(qb, qg, G, lane);
         }
     }
+    // The fragments go to shared memory (both consumer warps hold the same
+    // ones) and are read back per k-step: the 16 registers they would pin
+    // through the tile loop are what made the fused step spill.
+    const uint32_t q_lane = smem_u32(smem + Lay::kBodyBytes) + lane * 8;
+    if (warp == 0) {
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; ++kk)
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(q_lane + kk * 256), "r"(qb[kk][0]),
+                         "r"(qb[kk][1])
+                         : "memory");
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    auto qfrag = [&](int kk, uint32_t& b0, uint32_t& b1) { lds64(q_lane + kk * 256, b0, b1); };
     TileState<D> ts;
     ts.reset();
 
@@ -306,7 +322,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            attend_tile_fp8(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
+            attend_tile_fp8(ts, qfrag, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
                             scale_log2, lane, [&] { release_stage(&empty_bar[st], lane); });
         } else {
             if (kMode == kModeStep && it == new_tile) {
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            attend_tile<T, D>(ts, qb, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
+            attend_tile<T, D>(ts, qfrag, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
                               scale_log2, lane);
             release_stage(&empty_bar[st], lane);
         }

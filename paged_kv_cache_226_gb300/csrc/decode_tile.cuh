@@ -102,6 +102,11 @@ __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
     return v;
 }
 
+// 8-byte shared-memory load (shared-window address).
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int j) {
     return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
@@ -163,11 +168,12 @@ __device__ __forceinline__ void put_code_chunk(uint8_t* tile, int r, int c, uint
     *reinterpret_cast<uint2*>(tile + r * 128 + (((c >> 1) ^ (r & 7)) << 4) + (c & 1) * 8) = codes;
 }
 
-// Attends one FP8 tile pair (tokens tok0 .. tok0+15, masked from t_end on).
+// Attends one FP8 tile pair (tokens tok0 .. tok0+15, masked from t_end on);
+// qfrag(kk, b0, b1) supplies the fp16 q^T fragments of k-step kk.
 // release() runs once the warp has read the staged codes into registers, so
 // the stage can be refilled while the P V products run.
-template <typename Release>
-__device__ __forceinline__ void attend_tile_fp8(TileState<128>& s, const uint32_t (&qb)[8][2],
+template <typename QFrag, typename Release>
+__device__ __forceinline__ void attend_tile_fp8(TileState<128>& s, QFrag&& qfrag,
                                                 const uint8_t* ktile, const uint8_t* vtile,
                                                 int tok0, int t_end, float scale_log2, int lane,
                                                 Release&& release) {
@@ -190,7 +196,9 @@ __device__ __forceinline__ void attend_tile_fp8(TileState<128>& s, const uint32_
         const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl >> 16));
         const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh & 0xffffu));
         const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh >> 16));
-        M::run(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        uint32_t b0, b1;
+        qfrag(kk, b0, b1);
+        M::run(sc, a0, a1, a2, a3, b0, b1);
     }
     // V: chunk r8 of token rows 2c4, 2c4+1, 2c4+8, 2c4+9; rows past the end are
     // cleared (they may hold stale codes, NaN among them)
@@ -262,11 +270,13 @@ __device__ __forceinline__ void put_tile_chunk(uint8_t* tile, int r, int c, uint
         val;
 }
 
+// qfrag(kk, b0, b1) supplies the q^T B-operand fragments of k-step kk (from
+// registers or from shared memory, as the caller keeps them).
 // Attends the 16 tokens tok0 .. tok0+15 of a tile; tokens >= t_end are masked
 // (their V rows are zeroed in shared memory, since they may hold stale
 // non-finite bits).
-template <typename T, int D>
-__device__ __forceinline__ void attend_tile(TileState<D>& s, const uint32_t (&qb)[D / 16][2],
+template <typename T, int D, typename QFrag>
+__device__ __forceinline__ void attend_tile(TileState<D>& s, QFrag&& qfrag,
                                             uint8_t* ktile, uint8_t* vtile, int tok0, int t_end,
                                             float scale_log2, int lane) {
     using M = Mma<T>;
@@ -292,7 +302,9 @@ __device__ __forceinline__ void attend_tile(TileState<D>& s, const uint32_t (&qb
                               (((chunk & 7) ^ (k_tok & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         ldsm_x4(addr, a0, a1, a2, a3);
-        M::run(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        uint32_t b0, b1;
+        qfrag(kk, b0, b1);
+        M::run(sc, a0, a1, a2, a3, b0, b1);
     }
 
     // mask past the span's end, scale into log2 units
