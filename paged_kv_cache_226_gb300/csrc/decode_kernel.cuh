@@ -302,29 +302,62 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         }
     }
 
-    for (int it = warp; it < n_tiles; it += kConsumerWarps) {
-        const int st = it % Lay::kRing;
-        bool ok = mbar_wait(&full_bar[st], (it / Lay::kRing) & 1, PA_DECODE_WAIT_LIMIT(p));
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
-            break;
-        }
-        uint8_t* ktile = smem + st * Lay::kStageBytes;
-        uint8_t* vtile = ktile + Lay::kTileBytes;
-        if constexpr (kFp8) {
-            if (kMode == kModeStep && it == new_tile) {
+    if constexpr (kFp8) {
+        // Consumer warp w takes the tile pairs (2i, 2i + 1), i = w, w + W, ...
+        // (W consumer warps); tile t sits in stage t % kRing, so with kRing a
+        // multiple of 2W every stage belongs to exactly one warp.
+        static_assert(Lay::kRing % (2 * kConsumerWarps) == 0, "FP8 stages must pair up per warp");
+        for (int it = 2 * warp; it < n_tiles; it += 2 * kConsumerWarps) {
+            const bool two = it + 1 < n_tiles;
+            const int st0 = it % Lay::kRing, st1 = (it + 1) % Lay::kRing;
+            bool ok = mbar_wait(&full_bar[st0], (it / Lay::kRing) & 1, PA_DECODE_WAIT_LIMIT(p));
+            if (ok && two)
+                ok = mbar_wait(&full_bar[st1], ((it + 1) / Lay::kRing) & 1, PA_DECODE_WAIT_LIMIT(p));
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            uint8_t* ktile0 = smem + st0 * Lay::kStageBytes;
+            uint8_t* vtile0 = ktile0 + Lay::kTileBytes;
+            uint8_t* ktile1 = smem + st1 * Lay::kStageBytes;
+            uint8_t* vtile1 = ktile1 + Lay::kTileBytes;
+            if (kMode == kModeStep && (it == new_tile || (two && it + 1 == new_tile))) {
                 // lanes 0-15: 8-code chunks of K, lanes 16-31: of V, into the staged codes
                 const int c = lane & 15;
                 const bool is_k = lane < 16;
+                const bool first = it == new_tile;
                 const uint4 cv = new_token_chunk<T, D, true>(p, b, g, new_slot, c, is_k);
-                put_code_chunk(is_k ? ktile : vtile, (L - 1) % kTileTokens, c,
-                               make_uint2(cv.x, cv.y));
+                put_code_chunk(is_k ? (first ? ktile0 : ktile1) : (first ? vtile0 : vtile1),
+                               (L - 1) % kTileTokens, c, make_uint2(cv.x, cv.y));
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            attend_tile_fp8(ts, qfrag, ktile, vtile, (tile_begin + it) * kTileTokens, t_end,
-                            scale_log2, lane, [&] { release_stage(&empty_bar[st], lane); });
-        } else {
+            const int tok0 = (tile_begin + it) * kTileTokens;
+            if (two) {
+                attend_pair_fp8(ts, qfrag, ktile0, vtile0, ktile1, vtile1, tok0, t_end, scale_log2,
+                                lane, [&] {
+                                    fence_proxy_async_smem();
+                                    __syncwarp();
+                                    if (lane == 0) {
+                                        mbar_arrive(&empty_bar[st0]);
+                                        mbar_arrive(&empty_bar[st1]);
+                                    }
+                                });
+            } else {
+                attend_tile_fp8(ts, qfrag, ktile0, vtile0, tok0, t_end, scale_log2, lane,
+                                [&] { release_stage(&empty_bar[st0], lane); });
+            }
+        }
+    } else {
+        for (int it = warp; it < n_tiles; it += kConsumerWarps) {
+            const int st = it % Lay::kRing;
+            bool ok = mbar_wait(&full_bar[st], (it / Lay::kRing) & 1, PA_DECODE_WAIT_LIMIT(p));
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) flag_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            uint8_t* ktile = smem + st * Lay::kStageBytes;
+            uint8_t* vtile = ktile + Lay::kTileBytes;
             if (kMode == kModeStep && it == new_tile) {
                 // lanes 0-15: 16-byte chunks of K, lanes 16-31: of V
                 const int c = lane & 15;

@@ -168,60 +168,62 @@ __device__ __forceinline__ void put_code_chunk(uint8_t* tile, int r, int c, uint
     *reinterpret_cast<uint2*>(tile + r * 128 + (((c >> 1) ^ (r & 7)) << 4) + (c & 1) * 8) = codes;
 }
 
-// Attends one FP8 tile pair (tokens tok0 .. tok0+15, masked from t_end on);
-// qfrag(kk, b0, b1) supplies the fp16 q^T fragments of k-step kk.
-// release() runs once the warp has read the staged codes into registers, so
-// the stage can be refilled while the P V products run.
-template <typename QFrag, typename Release>
-__device__ __forceinline__ void attend_tile_fp8(TileState<128>& s, QFrag&& qfrag,
-                                                const uint8_t* ktile, const uint8_t* vtile,
-                                                int tok0, int t_end, float scale_log2, int lane,
-                                                Release&& release) {
-    using M = Mma<__half>;
+// Pieces of the FP8 tile math.  K: lane (r8, c4) reads 16-byte chunks
+// 2c4, 2c4+1 of token rows r8 and r8 + 8 (same swizzle row phase); k-step kk
+// takes word kk & 3 of chunk kk >> 2.  V: chunk r8 of token rows 2c4, 2c4+1,
+// 2c4+8, 2c4+9, cleared for rows past the end (they may hold stale codes,
+// NaN among them).
+__device__ __forceinline__ void fp8_load_k(uint4 (&klo)[2], uint4 (&khi)[2], const uint8_t* ktile,
+                                           int lane) {
     const int r8 = lane >> 2, c4 = lane & 3;
-    // K: chunks 2c4, 2c4+1 of token rows r8 and r8 + 8 (same swizzle row phase)
-    uint4 klo[2], khi[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int off = (((2 * c4 + i) ^ r8) << 4);
         klo[i] = lds128(ktile + r8 * 128 + off);
         khi[i] = lds128(ktile + (r8 + 8) * 128 + off);
     }
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t wl = word_of(klo[kk >> 2], kk & 3);
-        const uint32_t wh = word_of(khi[kk >> 2], kk & 3);
-        const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl & 0xffffu));
-        const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl >> 16));
-        const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh & 0xffffu));
-        const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh >> 16));
-        uint32_t b0, b1;
-        qfrag(kk, b0, b1);
-        M::run(sc, a0, a1, a2, a3, b0, b1);
-    }
-    // V: chunk r8 of token rows 2c4, 2c4+1, 2c4+8, 2c4+9; rows past the end are
-    // cleared (they may hold stale codes, NaN among them)
-    uint4 v[4];
+}
+
+__device__ __forceinline__ void fp8_score_step(float (&sc)[4], const uint4 (&klo)[2],
+                                               const uint4 (&khi)[2], int kk, uint32_t b0,
+                                               uint32_t b1) {
+    const uint32_t wl = word_of(klo[kk >> 2], kk & 3);
+    const uint32_t wh = word_of(khi[kk >> 2], kk & 3);
+    const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl & 0xffffu));
+    const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl >> 16));
+    const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh & 0xffffu));
+    const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh >> 16));
+    Mma<__half>::run(sc, a0, a1, a2, a3, b0, b1);
+}
+
+__device__ __forceinline__ void fp8_load_v(uint4 (&v)[4], const uint8_t* vtile, int tok0,
+                                           int t_end, int lane) {
+    const int r8 = lane >> 2, c4 = lane & 3;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int t = 2 * c4 + (i & 1) + 8 * (i >> 1);
         v[i] = lds128(vtile + t * 128 + ((r8 ^ (t & 7)) << 4));
         if (tok0 + t >= t_end) v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
-    release();
+}
 
-    const bool v_lo = tok0 + r8 < t_end, v_hi8 = tok0 + r8 + 8 < t_end;
-    const float x0 = v_lo ? sc[0] * scale_log2 : -INFINITY;
-    const float x1 = v_lo ? sc[1] * scale_log2 : -INFINITY;
-    const float x2 = v_hi8 ? sc[2] * scale_log2 : -INFINITY;
-    const float x3 = v_hi8 ? sc[3] * scale_log2 : -INFINITY;
-    float xa = fmaxf(x0, x2), xb = fmaxf(x1, x3);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
-        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, o));
-    }
+// O^T slab n += V^T . P^T from the staged codes (two tokens' bytes paired by prmt).
+__device__ __forceinline__ void fp8_pv_slab(float (&acc)[4], const uint4 (&v)[4], int n,
+                                            uint32_t pb0, uint32_t pb1) {
+    const int j = n >> 1;
+    const uint32_t sel = (n & 1) ? 0x7362u : 0x5140u;   // bytes (2h, 2h+1) of two tokens
+    const uint32_t x01 = prmt(word_of(v[0], j), word_of(v[1], j), sel);
+    const uint32_t x23 = prmt(word_of(v[2], j), word_of(v[3], j), sel);
+    const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xffffu));
+    const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16));
+    const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 & 0xffffu));
+    const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 >> 16));
+    Mma<__half>::run(acc, a0, a1, a2, a3, pb0, pb1);
+}
+
+// Raises the reference maxima when this step's maxima xa, xb (log2 units, per
+// head pair, already reduced over the warp) exceed them by more than 2^8.
+__device__ __forceinline__ void fp8_raise(TileState<128>& s, float xa, float xb) {
     s.tA = fmaxf(s.tA, xa);
     s.tB = fmaxf(s.tB, xb);
     const bool raiseA = xa > s.mA + kRescaleThresholdLog2;
@@ -241,26 +243,114 @@ __device__ __forceinline__ void attend_tile_fp8(TileState<128>& s, QFrag&& qfrag
         s.mA = nA;
         s.mB = nB;
     }
-    const uint32_t p01 = M::pack(ex2(x0 - s.mA), ex2(x1 - s.mB));
-    const uint32_t p23 = M::pack(ex2(x2 - s.mA), ex2(x3 - s.mB));
-    {
-        const float2 u = M::unpack(p01), w = M::unpack(p23);
-        s.lA += u.x + w.x;
-        s.lB += u.y + w.y;
+}
+
+// Masked, scaled scores (r8 / r8 + 8 rows, heads hA / hB) of a tile at tok0.
+__device__ __forceinline__ void fp8_mask(float (&x)[4], const float (&sc)[4], int tok0, int t_end,
+                                         float scale_log2, int lane) {
+    const int r8 = lane >> 2;
+    const bool v_lo = tok0 + r8 < t_end, v_hi8 = tok0 + r8 + 8 < t_end;
+    x[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
+    x[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
+    x[2] = v_hi8 ? sc[2] * scale_log2 : -INFINITY;
+    x[3] = v_hi8 ? sc[3] * scale_log2 : -INFINITY;
+}
+
+// P of a tile in fp16 (added into the row sums), transposed into P^T fragments.
+__device__ __forceinline__ void fp8_probs(TileState<128>& s, const float (&x)[4], uint32_t& pb0,
+                                          uint32_t& pb1) {
+    using M = Mma<__half>;
+    const uint32_t p01 = M::pack(ex2(x[0] - s.mA), ex2(x[1] - s.mB));
+    const uint32_t p23 = M::pack(ex2(x[2] - s.mA), ex2(x[3] - s.mB));
+    const float2 u = M::unpack(p01), w = M::unpack(p23);
+    s.lA += u.x + w.x;
+    s.lB += u.y + w.y;
+    pb0 = movmatrix_trans(p01);
+    pb1 = movmatrix_trans(p23);
+}
+
+__device__ __forceinline__ void warp_max_pairs(float& xa, float& xb) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
+        xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, o));
     }
-    const uint32_t pb0 = movmatrix_trans(p01);
-    const uint32_t pb1 = movmatrix_trans(p23);
+}
+
+// Attends one FP8 tile (tokens tok0 .. tok0+15, masked from t_end on);
+// qfrag(kk, b0, b1) supplies the fp16 q^T fragments of k-step kk.
+// release() runs once the warp has read the staged codes into registers, so
+// the stage can be refilled while the P V products run.
+template <typename QFrag, typename Release>
+__device__ __forceinline__ void attend_tile_fp8(TileState<128>& s, QFrag&& qfrag,
+                                                const uint8_t* ktile, const uint8_t* vtile,
+                                                int tok0, int t_end, float scale_log2, int lane,
+                                                Release&& release) {
+    uint4 klo[2], khi[2];
+    fp8_load_k(klo, khi, ktile, lane);
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1;
+        qfrag(kk, b0, b1);
+        fp8_score_step(sc, klo, khi, kk, b0, b1);
+    }
+    uint4 v[4];
+    fp8_load_v(v, vtile, tok0, t_end, lane);
+    release();
+
+    float x[4];
+    fp8_mask(x, sc, tok0, t_end, scale_log2, lane);
+    float xa = fmaxf(x[0], x[2]), xb = fmaxf(x[1], x[3]);
+    warp_max_pairs(xa, xb);
+    fp8_raise(s, xa, xb);
+    uint32_t pb0, pb1;
+    fp8_probs(s, x, pb0, pb1);
+#pragma unroll
+    for (int n = 0; n < 8; ++n) fp8_pv_slab(s.acc[n], v, n, pb0, pb1);
+}
+
+// Attends two FP8 tiles at once: tile 0 (tokens tok0 .. tok0+15) and tile 1
+// (the next 16), both masked from t_end on.  Their score chains interleave,
+// one max reduction and one rescale test cover both, and each accumulator
+// slab takes both P V products, so the per-tile chain of dependent steps is
+// about halved.  release() runs once both tiles' codes are in registers.
+template <typename QFrag, typename Release>
+__device__ __forceinline__ void attend_pair_fp8(TileState<128>& s, QFrag&& qfrag,
+                                                const uint8_t* ktile0, const uint8_t* vtile0,
+                                                const uint8_t* ktile1, const uint8_t* vtile1,
+                                                int tok0, int t_end, float scale_log2, int lane,
+                                                Release&& release) {
+    uint4 klo0[2], khi0[2], klo1[2], khi1[2];
+    fp8_load_k(klo0, khi0, ktile0, lane);
+    fp8_load_k(klo1, khi1, ktile1, lane);
+    float sc0[4] = {0.f, 0.f, 0.f, 0.f}, sc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1;
+        qfrag(kk, b0, b1);
+        fp8_score_step(sc0, klo0, khi0, kk, b0, b1);
+        fp8_score_step(sc1, klo1, khi1, kk, b0, b1);
+    }
+    uint4 v0[4], v1[4];
+    fp8_load_v(v0, vtile0, tok0, t_end, lane);
+    fp8_load_v(v1, vtile1, tok0 + kTileTokens, t_end, lane);
+    release();
+
+    float x[4], y[4];
+    fp8_mask(x, sc0, tok0, t_end, scale_log2, lane);
+    fp8_mask(y, sc1, tok0 + kTileTokens, t_end, scale_log2, lane);
+    float xa = fmaxf(fmaxf(x[0], x[2]), fmaxf(y[0], y[2]));
+    float xb = fmaxf(fmaxf(x[1], x[3]), fmaxf(y[1], y[3]));
+    warp_max_pairs(xa, xb);
+    fp8_raise(s, xa, xb);
+    uint32_t pb0, pb1, qb0, qb1;
+    fp8_probs(s, x, pb0, pb1);
+    fp8_probs(s, y, qb0, qb1);
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
-        const int j = n >> 1;
-        const uint32_t sel = (n & 1) ? 0x7362u : 0x5140u;   // bytes (2h, 2h+1) of two tokens
-        const uint32_t x01 = prmt(word_of(v[0], j), word_of(v[1], j), sel);
-        const uint32_t x23 = prmt(word_of(v[2], j), word_of(v[3], j), sel);
-        const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xffffu));
-        const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16));
-        const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 & 0xffffu));
-        const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 >> 16));
-        M::run(s.acc[n], a0, a1, a2, a3, pb0, pb1);
+        fp8_pv_slab(s.acc[n], v0, n, pb0, pb1);
+        fp8_pv_slab(s.acc[n], v1, n, qb0, qb1);
     }
 }
 
