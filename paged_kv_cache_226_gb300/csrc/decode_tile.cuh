@@ -187,12 +187,9 @@ __device__ __forceinline__ void fp8_load_k(uint4 (&klo)[2], uint4 (&khi)[2], con
 __device__ __forceinline__ void fp8_score_step(float (&sc)[4], const uint4 (&klo)[2],
                                                const uint4 (&khi)[2], int kk, uint32_t b0,
                                                uint32_t b1) {
-    const uint32_t wl = word_of(klo[kk >> 2], kk & 3);
-    const uint32_t wh = word_of(khi[kk >> 2], kk & 3);
-    const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl & 0xffffu));
-    const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(wl >> 16));
-    const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh & 0xffffu));
-    const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(wh >> 16));
+    uint32_t a0, a1, a2, a3;
+    e4m3x4_to_f16x2x2(word_of(klo[kk >> 2], kk & 3), a0, a2);
+    e4m3x4_to_f16x2x2(word_of(khi[kk >> 2], kk & 3), a1, a3);
     Mma<__half>::run(sc, a0, a1, a2, a3, b0, b1);
 }
 
@@ -203,7 +200,11 @@ __device__ __forceinline__ void fp8_load_v(uint4 (&v)[4], const uint8_t* vtile, 
     for (int i = 0; i < 4; ++i) {
         const int t = 2 * c4 + (i & 1) + 8 * (i >> 1);
         v[i] = lds128(vtile + t * 128 + ((r8 ^ (t & 7)) << 4));
-        if (tok0 + t >= t_end) v[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tok0 + kTileTokens > t_end) {               // ragged tail only (warp-uniform)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (tok0 + 2 * c4 + (i & 1) + 8 * (i >> 1) >= t_end) v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -214,10 +215,9 @@ __device__ __forceinline__ void fp8_pv_slab(float (&acc)[4], const uint4 (&v)[4]
     const uint32_t sel = (n & 1) ? 0x7362u : 0x5140u;   // bytes (2h, 2h+1) of two tokens
     const uint32_t x01 = prmt(word_of(v[0], j), word_of(v[1], j), sel);
     const uint32_t x23 = prmt(word_of(v[2], j), word_of(v[3], j), sel);
-    const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xffffu));
-    const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16));
-    const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 & 0xffffu));
-    const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 >> 16));
+    uint32_t a0, a1, a2, a3;
+    e4m3x4_to_f16x2x2(x01, a0, a1);
+    e4m3x4_to_f16x2x2(x23, a2, a3);
     Mma<__half>::run(acc, a0, a1, a2, a3, pb0, pb1);
 }
 
@@ -248,12 +248,13 @@ __device__ __forceinline__ void fp8_raise(TileState<128>& s, float xa, float xb)
 // Masked, scaled scores (r8 / r8 + 8 rows, heads hA / hB) of a tile at tok0.
 __device__ __forceinline__ void fp8_mask(float (&x)[4], const float (&sc)[4], int tok0, int t_end,
                                          float scale_log2, int lane) {
-    const int r8 = lane >> 2;
-    const bool v_lo = tok0 + r8 < t_end, v_hi8 = tok0 + r8 + 8 < t_end;
-    x[0] = v_lo ? sc[0] * scale_log2 : -INFINITY;
-    x[1] = v_lo ? sc[1] * scale_log2 : -INFINITY;
-    x[2] = v_hi8 ? sc[2] * scale_log2 : -INFINITY;
-    x[3] = v_hi8 ? sc[3] * scale_log2 : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = sc[i] * scale_log2;
+    if (tok0 + kTileTokens > t_end) {               // ragged tail only (warp-uniform)
+        const int r8 = lane >> 2;
+        if (tok0 + r8 >= t_end) x[0] = x[1] = -INFINITY;
+        if (tok0 + r8 + 8 >= t_end) x[2] = x[3] = -INFINITY;
+    }
 }
 
 // P of a tile in fp16 (added into the row sums), transposed into P^T fragments.

@@ -235,6 +235,18 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     return r;
 }
 
+// Four E4M3 codes (byte i of w) to fp16, exactly: lo = bytes 0, 1 and hi =
+// bytes 2, 3 (higher byte -> higher half).  The word is split into its two
+// 16-bit halves as register halves, with no shift or mask instruction.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 // Nearest E4M3 codes (ties to even, saturating at +-448) of two floats; hi
 // lands in the high byte.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float hi, float lo) {
