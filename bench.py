@@ -525,11 +525,14 @@ def bench_ours(args):
     tm = time_steps(plan, flush, dev, stream, args.steps, args.warmup, local_rank, world)
     errs = lib.read_device_errors(dev)
 
-    # End to end through the public API: every step copies its inputs from
-    # pinned host memory (one packed copy, lib.InputStaging), runs the
-    # layer-step and reads the output back; the events bracket copies +
-    # kernels + the host's launch work (the L2 flush before each step is
-    # outside them).
+    # End to end through the public API, with the step's inputs in pinned host
+    # memory and its output read back there every step, inside the events
+    # (the L2 flush before each step is outside them; the host synchronises
+    # after every step).  Headline form: the fused step reads q, the new K/V,
+    # slots, tables and lengths straight from the pinned host buffers and
+    # stores its output into pinned host memory (unified addressing over the
+    # host link; no copy launch).  Also timed: the staged form, one packed
+    # upload kernel, the step on device buffers, one read-back kernel.
     e2e = None
     if not args.no_e2e:
         names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
@@ -539,35 +542,59 @@ def bench_ours(args):
         for k, t in src.items():
             stage.h[k].copy_(t)
         scales = dict(k_scale=FP8_K_SCALE, v_scale=FP8_V_SCALE) if args.kv_dtype == "fp8" else {}
+        h2d = stage.nbytes
+        n_e2e = min(args.steps, 200)
+
+        def e2e_time(plan):
+            e_ms = []
+            for it in range(args.warmup + n_e2e):
+                flush(0.5)
+                ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ea.record(stream)
+                plan.replay()
+                eb.record(stream)
+                stream.synchronize()
+                if it >= args.warmup:
+                    e_ms.append(ea.elapsed_time(eb))
+            return max_over_ranks(sum(e_ms) / len(e_ms), dev)
+
+        forms = {}
+        if mode == "fused":
+            out_h = torch.empty(tuple(src["q"].shape), dtype=src["q"].dtype).pin_memory()
+            plan_zc = lib.StepPlan(stage.h["q"], stage.h["k_new"], stage.h["v_new"],
+                                   stage.h["slot_mapping"], d["k_cache"], d["v_cache"],
+                                   stage.h["block_tables"], stage.h["context_lens"], w.scale,
+                                   max_len, out=out_h, mode=mode, partition_size=partition,
+                                   **scales)
+            plan_zc.capture_graph()
+            forms["zero_copy"] = (e2e_time(plan_zc), out_h.numel() * out_h.element_size(),
+                                  "none: the fused step reads its inputs from the pinned host "
+                                  "buffers and stores its output into pinned host memory",
+                                  "one CUDA graph per step (the layer-step)")
+            del plan_zc
         plan_e2e = lib.StepPlan(stage.d["q"], stage.d["k_new"], stage.d["v_new"],
                                 stage.d["slot_mapping"], d["k_cache"], d["v_cache"],
                                 stage.d["block_tables"], stage.d["context_lens"], w.scale,
                                 max_len, mode=mode, partition_size=partition, **scales)
-        out_h = torch.empty(plan_e2e.out.shape, dtype=plan_e2e.out.dtype).pin_memory()
-        h2d = stage.nbytes
-        d2h = out_h.numel() * out_h.element_size()
-        # one CUDA graph per step: upload, layer-step, read-back
+        out_s = torch.empty(plan_e2e.out.shape, dtype=plan_e2e.out.dtype).pin_memory()
         plan_e2e.capture_graph(before=stage.upload,
-                               after=lambda: lib.copy_async(out_h, plan_e2e.out))
-        n_e2e = min(args.steps, 200)
-        e_ms = []
-        for it in range(args.warmup + n_e2e):
-            flush(0.5)
-            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ea.record(stream)
-            plan_e2e.replay()
-            eb.record(stream)
-            stream.synchronize()
-            if it >= args.warmup:
-                e_ms.append(ea.elapsed_time(eb))
-        e2e_ms = max_over_ranks(sum(e_ms) / len(e_ms), dev)
+                               after=lambda: lib.copy_async(out_s, plan_e2e.out))
+        forms["staged"] = (e2e_time(plan_e2e), out_s.numel() * out_s.element_size(),
+                           "1 host-to-device (inputs packed), 1 device-to-host (out), each a "
+                           "short kernel on pinned host memory (pa_copy_async)",
+                           "one CUDA graph per step (upload, layer-step, read-back)")
+        del plan_e2e, stage
+        head = "zero_copy" if "zero_copy" in forms else "staged"
+        e2e_ms, d2h, copies, launch = forms[head]
         e2e = {"value": round(whole_job_gbs(nb["layer_step"], world, e2e_ms), 3),
                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_ms, 5), "steps": n_e2e,
-               "copies_per_step": "1 host-to-device (inputs packed), 1 device-to-host (out), "
-                                  "each a short kernel on pinned host memory (pa_copy_async)",
-               "launch": "one CUDA graph per step (upload, layer-step, read-back)"}
-        del plan_e2e, stage
+               "ms_per_step": round(e2e_ms, 5), "steps": n_e2e, "form": head,
+               "copies_per_step": copies, "launch": launch}
+        for name, (ms, _, copies, launch) in forms.items():
+            if name != head:
+                e2e[name] = {"value": round(whole_job_gbs(nb["layer_step"], world, ms), 3),
+                             "ms_per_step": round(ms, 5), "copies_per_step": copies,
+                             "launch": launch}
 
     hbm, peak_src = peaks()
     summ = decode_summary(w, mode, partition, args.kv_dtype, nb, tm, dev, world, hbm, peak_src,

@@ -211,7 +211,8 @@ int pa_decode_split_fp8(const void* q, const void* k_cache, const void* v_cache,
                         int32_t max_num_partitions, float* tmp_out, float* max_logits,
                         float* exp_sums, const pa_shape* shp, void* stream);
 
-/* pa_decode_step over an E4M3 cache: the new token is quantised as in
+/* pa_decode_step over an E4M3 cache (the same memory rules, pinned host
+ * inputs and output included): the new token is quantised as in
  * pa_reshape_and_cache_fp8 and attention reads the quantised values. */
 int pa_decode_step_fp8(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
                        void* k_cache, void* v_cache, const int32_t* block_tables,
@@ -391,8 +392,13 @@ int pa_decode_static_workspace(const void* q, const void* k_cache, const void* v
  * stages its weights in shared memory: (Hq/Hkv) * (max_num_partitions + 1)
  * must not exceed 2096 at head_dim 128 or 1072 at head_dim 64, else
  * PA_ERR_UNSUPPORTED.  out [B][Hq][D] receives the
- * attention output.  All pointers device; k, v, out, tmp_out, max_logits,
- * exp_sums 16-byte aligned; errors as pa_decode_split.
+ * attention output.  k_cache, v_cache and the workspace are device memory;
+ * q, k, v, slot_mapping, block_tables, context_lens and out may be device
+ * memory or pinned host memory that the device reaches through unified
+ * addressing (each CTA reads its inputs and writes its output directly, so
+ * a step needs no separate upload or read-back; on a Grace-Blackwell node
+ * this moves them over the coherent host link).  k, v, out, tmp_out,
+ * max_logits, exp_sums 16-byte aligned; errors as pa_decode_split.
  */
 int pa_decode_step(const void* q, const void* k, const void* v, const int64_t* slot_mapping,
                    void* k_cache, void* v_cache, const int32_t* block_tables,

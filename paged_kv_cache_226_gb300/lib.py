@@ -136,16 +136,19 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
-def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+def _need(t: torch.Tensor, name: str, dtype=None, device=None, host_ok: bool = False):
+    """Checks a tensor argument; with ``host_ok`` a pinned host tensor is
+    accepted too (the kernel reaches it through unified addressing)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    pinned_host = host_ok and not t.is_cuda and t.is_pinned()
+    if not t.is_cuda and not pinned_host:
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if device is not None and t.device != device:
+    if device is not None and t.is_cuda and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
@@ -178,13 +181,13 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
                                     _ptr(v_cache), T, ctypes.byref(shp), _stream_handle(dev)))
 
 
-def _decode_common(q, k_cache, v_cache, block_tables, context_lens):
+def _decode_common(q, k_cache, v_cache, block_tables, context_lens, host_ok: bool = False):
     dev = k_cache.device
-    _need(q, "q", k_cache.dtype, dev)
+    _need(q, "q", k_cache.dtype, dev, host_ok)
     _need(k_cache, "k_cache", None, dev)
     _need(v_cache, "v_cache", k_cache.dtype, dev)
-    _need(block_tables, "block_tables", torch.int32, dev)
-    _need(context_lens, "context_lens", torch.int32, dev)
+    _need(block_tables, "block_tables", torch.int32, dev, host_ok)
+    _need(context_lens, "context_lens", torch.int32, dev, host_ok)
     if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
         raise ValueError("caches must be [num_blocks][block_size][num_kv_heads][head_dim]")
     B, hq, d = q.shape
@@ -213,13 +216,15 @@ def num_partitions(max_context_len: int, partition_size: int = DEFAULT_PARTITION
     return max(1, -(-int(max_context_len) // int(partition_size)))
 
 
-def split_workspace(q: torch.Tensor, max_num_partitions: int
+def split_workspace(q: torch.Tensor, max_num_partitions: int, device=None
                     ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """Allocate (tmp_out, max_logits, exp_sums) for the split path."""
+    """Allocate (tmp_out, max_logits, exp_sums) for the split path (on
+    ``device``, default q's)."""
     B, hq, d = q.shape
-    tmp = torch.empty((B, hq, max_num_partitions, d), dtype=torch.float32, device=q.device)
-    ml = torch.empty((B, hq, max_num_partitions), dtype=torch.float32, device=q.device)
-    es = torch.empty((B, hq, max_num_partitions), dtype=torch.float32, device=q.device)
+    device = q.device if device is None else device
+    tmp = torch.empty((B, hq, max_num_partitions, d), dtype=torch.float32, device=device)
+    ml = torch.empty((B, hq, max_num_partitions), dtype=torch.float32, device=device)
+    es = torch.empty((B, hq, max_num_partitions), dtype=torch.float32, device=device)
     return tmp, ml, es
 
 
@@ -366,13 +371,13 @@ def reshape_and_cache_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale: float,
                                         ctypes.byref(shp), _stream_handle(dev)))
 
 
-def _fp8_common(q, k_cache, v_cache, block_tables, context_lens):
+def _fp8_common(q, k_cache, v_cache, block_tables, context_lens, host_ok: bool = False):
     dev = k_cache.device
-    _need(q, "q", q.dtype, dev)
+    _need(q, "q", q.dtype, dev, host_ok)
     _need(k_cache, "k_cache", torch.uint8, dev)
     _need(v_cache, "v_cache", torch.uint8, dev)
-    _need(block_tables, "block_tables", torch.int32, dev)
-    _need(context_lens, "context_lens", torch.int32, dev)
+    _need(block_tables, "block_tables", torch.int32, dev, host_ok)
+    _need(context_lens, "context_lens", torch.int32, dev, host_ok)
     if q.dtype not in _DTYPE_CODES:
         raise TypeError("q must be float16 or bfloat16")
     if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
@@ -438,11 +443,13 @@ def decode_step_fp8(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table
     return out
 
 
-def step_workspace(q: torch.Tensor, num_kv_heads: int, max_num_partitions: int):
-    """(tmp_out, max_logits, exp_sums, counters) for ``decode_step``; the
-    counters start at zero and every step leaves them at zero."""
-    tmp, ml, es = split_workspace(q, max_num_partitions)
-    counters = torch.zeros((q.shape[0], num_kv_heads), dtype=torch.int32, device=q.device)
+def step_workspace(q: torch.Tensor, num_kv_heads: int, max_num_partitions: int, device=None):
+    """(tmp_out, max_logits, exp_sums, counters) for ``decode_step`` (on
+    ``device``, default q's); the counters start at zero and every step leaves
+    them at zero."""
+    device = q.device if device is None else device
+    tmp, ml, es = split_workspace(q, max_num_partitions, device)
+    counters = torch.zeros((q.shape[0], num_kv_heads), dtype=torch.int32, device=device)
     return tmp, ml, es, counters
 
 
@@ -709,6 +716,13 @@ class StepPlan:
     (``capture_graph``).  The tensors must stay alive and keep their shapes;
     their contents (new tokens, tables, lengths) may change between steps as
     long as ``context_lens`` stays within ``max_context_len``.
+
+    In the fused mode q, k_new, v_new, slot_mapping, block_tables,
+    context_lens and out may be pinned host tensors: the kernel reads the
+    inputs and writes the output over the host link through unified
+    addressing, with no copy launch (on a Grace-Blackwell node the fastest
+    way to move a step's inputs in and its output out).  The caches and the
+    workspace stay in device memory.
     """
 
     def __init__(self, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
@@ -717,27 +731,28 @@ class StepPlan:
                  k_scale: Optional[float] = None, v_scale: Optional[float] = None):
         self._lib = load()
         self.fp8 = k_cache.dtype == torch.uint8
-        if self.fp8:
-            if k_scale is None or v_scale is None:
-                raise ValueError("an FP8 cache needs k_scale and v_scale")
-            if mode not in ("auto", "fused", "balanced"):
-                raise ValueError("StepPlan runs an FP8 cache through the fused steps only")
-            shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens)
-        else:
-            shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens)
-        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
-            _need(t, n, q.dtype, dev)
-        _need(slot_mapping, "slot_mapping", torch.int64, dev)
-        T = slot_mapping.shape[0]
-        if k_new.shape != (T, k_cache.shape[2], k_cache.shape[3]) or v_new.shape != k_new.shape:
-            raise ValueError("k_new and v_new must be [num_tokens][num_kv_heads][head_dim]")
-        self.device = dev
-        self.out = torch.empty_like(q) if out is None else out
-        _need(self.out, "out", q.dtype, dev)
         if mode == "auto":
             mode = "fused"
         if mode not in ("single", "split", "fused", "balanced"):
             raise ValueError(f"unknown mode {mode!r}")
+        host_ok = mode == "fused"            # pinned host inputs / output allowed
+        if self.fp8:
+            if k_scale is None or v_scale is None:
+                raise ValueError("an FP8 cache needs k_scale and v_scale")
+            if mode not in ("fused", "balanced"):
+                raise ValueError("StepPlan runs an FP8 cache through the fused steps only")
+            shp, dev = _fp8_common(q, k_cache, v_cache, block_tables, context_lens, host_ok)
+        else:
+            shp, dev = _decode_common(q, k_cache, v_cache, block_tables, context_lens, host_ok)
+        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+            _need(t, n, q.dtype, dev, host_ok)
+        _need(slot_mapping, "slot_mapping", torch.int64, dev, host_ok)
+        T = slot_mapping.shape[0]
+        if k_new.shape != (T, k_cache.shape[2], k_cache.shape[3]) or v_new.shape != k_new.shape:
+            raise ValueError("k_new and v_new must be [num_tokens][num_kv_heads][head_dim]")
+        self.device = dev
+        self.out = torch.empty(q.shape, dtype=q.dtype, device=dev) if out is None else out
+        _need(self.out, "out", q.dtype, dev, host_ok)
         if mode in ("fused", "balanced") and T != q.shape[0]:
             raise ValueError("the fused step takes exactly one new token per sequence")
         self.mode = mode
@@ -765,7 +780,7 @@ class StepPlan:
                                _ptr(self.out), sref)
         elif mode == "fused":
             if workspace is None:
-                workspace = step_workspace(q, k_cache.shape[2], self.num_partitions)
+                workspace = step_workspace(q, k_cache.shape[2], self.num_partitions, dev)
             tmp, ml, es, counters = workspace
             self.workspace = workspace
             self._keep += list(workspace)

@@ -107,3 +107,55 @@ def test_copy_async_between_pinned_host_and_device(dev):
         lib.copy_async(d1[1:5], src[1:5])          # 4-byte aligned, not 16
     with pytest.raises(ValueError):
         lib.copy_async(d1, torch.empty(n // 4, dtype=torch.int32))   # pageable host memory
+
+
+@pytest.mark.parametrize("cache", ["fp16", "fp8"])
+def test_fused_step_with_pinned_host_inputs_and_output(dev, cache):
+    """The fused step reading q, the new K/V, slots, tables and lengths from
+    pinned host memory and writing its output there gives the device-memory
+    step's output and cache bits exactly, step after step (the host inputs
+    change between steps, as a serving loop writes them)."""
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=7, lens=[1, 16, 17, 300, 1024, 1500,
+                                                                       2049],
+                                       num_q_heads=32, num_kv_heads=8, head_dim=128,
+                                       block_size=16), seed=41)
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    src = {k: (torch.from_numpy(getattr(w, k)) if isinstance(getattr(w, k), np.ndarray)
+               else getattr(w, k)) for k in names}
+    host = {k: t.clone().pin_memory() for k, t in src.items()}
+    devt = {k: t.to(dev) for k, t in src.items()}
+    scales = {}
+    if cache == "fp8":
+        rng = np.random.default_rng(5)
+        kc1 = pin.fp8_codes(rng, tuple(w.k_cache.shape), 1 / 64).to(dev)
+        vc1 = pin.fp8_codes(rng, tuple(w.v_cache.shape), 1 / 48).to(dev)
+        scales = dict(k_scale=1 / 64, v_scale=1 / 48)
+    else:
+        kc1, vc1 = w.k_cache.to(dev), w.v_cache.to(dev)
+    kc2, vc2 = kc1.clone(), vc1.clone()
+    max_len = int(w.context_lens.max())
+    out_h = torch.zeros(tuple(src["q"].shape), dtype=src["q"].dtype).pin_memory()
+    zero_copy = lib.StepPlan(host["q"], host["k_new"], host["v_new"], host["slot_mapping"], kc1,
+                             vc1, host["block_tables"], host["context_lens"], w.scale, max_len,
+                             out=out_h, mode="fused", partition_size=512, **scales)
+    on_dev = lib.StepPlan(devt["q"], devt["k_new"], devt["v_new"], devt["slot_mapping"], kc2, vc2,
+                          devt["block_tables"], devt["context_lens"], w.scale, max_len,
+                          mode="fused", partition_size=512, **scales)
+    for step in range(3):
+        q = src["q"] * (1.0 + 0.5 * step)
+        host["q"].copy_(q)
+        devt["q"].copy_(q.to(dev))
+        zero_copy()
+        on_dev()
+        torch.cuda.synchronize(dev)
+        assert torch.equal(out_h.view(torch.int16), on_dev.out.cpu().view(torch.int16)), step
+        assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
+    with pytest.raises(ValueError):              # pageable host memory is refused
+        lib.StepPlan(src["q"], host["k_new"], host["v_new"], host["slot_mapping"], kc1, vc1,
+                     host["block_tables"], host["context_lens"], w.scale, max_len, out=out_h,
+                     mode="fused", **scales)
+    with pytest.raises(ValueError):              # host inputs only in the fused mode
+        lib.StepPlan(host["q"], host["k_new"], host["v_new"], host["slot_mapping"], kc1, vc1,
+                     host["block_tables"], host["context_lens"], w.scale, max_len, out=out_h,
+                     mode="split")
+    assert lib.read_device_errors(dev) == 0
