@@ -461,71 +461,64 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
     if (kMode == kModeStep && parts > 1) {
         // The last CTA of the (sequence, KV head) to finish merges all
         // partitions: M = max m_s, w_s = l_s e^(m_s - M), out = sum w_s o_s / sum w_s.
-        __threadfence();                                   // partials before the count
+        // Its chain is on the launch's critical path (the longest partition
+        // of a sequence finishes last), so it is kept to two round trips:
+        // the count, then every partition's record loaded at once.
+        // Release / acquire: the barrier orders this CTA's partial-record
+        // writes before thread 0's acq_rel add, and the add that sees
+        // parts - 1 acquires every other partition's records for the threads
+        // that pass the next barrier.
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
         int* counter = p.counters + (size_t)b * p.num_kv_heads + g;
-        if (tid == 0) merge_here = (atomicAdd(counter, 1) == parts - 1);
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        if (!merge_here) return;
-        __threadfence();                                   // other CTAs' partials visible
-        const size_t qh0 = (size_t)b * p.num_q_heads + (size_t)g * G;
-        // weights w[h][s] (natural-log units) into the merge area; one warp per head
-        float* wts = mrg;                                  // [G][parts]
-        float* dens = mrg + G * parts;                     // [G]
-        for (int h = warp; h < G; h += kConsumerWarps) {
-            const float* ml = p.max_logits + (qh0 + h) * p.max_parts;
-            const float* es = p.exp_sums + (qh0 + h) * p.max_parts;
-            float mx = -INFINITY;
-            for (int s2 = lane; s2 < parts; s2 += 32) mx = fmaxf(mx, __ldcg(ml + s2));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            float dsum = 0.f;
-            for (int s2 = lane; s2 < parts; s2 += 32) {
-                const float wv = __ldcg(es + s2) * __expf(__ldcg(ml + s2) - mx);
-                wts[h * parts + s2] = wv;
-                dsum += wv;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-            if (lane == 0) dens[h] = dsum;
+        if (tid == 0) {
+            int before;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                         : "=r"(before)
+                         : "l"(counter)
+                         : "memory");
+            merge_here = before == parts - 1;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        if (!merge_here) return;
+        const size_t qh0 = (size_t)b * p.num_q_heads + (size_t)g * G;
         for (int item = tid; item < items; item += kConsumerWarps * 32) {
             const int h = item / (D / 4);
             const int d = (item - h * (D / 4)) * 4;
+            const float* ml = p.max_logits + (qh0 + h) * p.max_parts;
+            const float* es = p.exp_sums + (qh0 + h) * p.max_parts;
             const float* src = p.tmp_out + (qh0 + h) * p.max_parts * D + d;
-            const float* wh = wts + h * parts;
-            // four partitions in flight per thread
-            float4 acc4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            int s2 = 0;
-            for (; s2 + 4 <= parts; s2 += 4) {
-                float4 x[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    x[j] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(s2 + j) * D));
+            // partitions four at a time, each group's loads issued together,
+            // folded in with a running maximum (natural-log units)
+            float mx = -INFINITY, den = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < parts; s0 += 4) {
+                float mj[4], ej[4];
+                float4 xj[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float wj = wh[s2 + j];
-                    acc4[j].x += wj * x[j].x; acc4[j].y += wj * x[j].y;
-                    acc4[j].z += wj * x[j].z; acc4[j].w += wj * x[j].w;
+                    const bool in = s0 + j < parts;
+                    mj[j] = in ? __ldcg(ml + s0 + j) : -INFINITY;
+                    ej[j] = in ? __ldcg(es + s0 + j) : 0.f;
+                    xj[j] = in ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)(s0 + j) * D))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                const float nm = fmaxf(fmaxf(mx, fmaxf(mj[0], mj[1])), fmaxf(mj[2], mj[3]));
+                const float keep = __expf(mx - nm);               // 0 on the first group
+                den *= keep;
+                acc.x *= keep; acc.y *= keep; acc.z *= keep; acc.w *= keep;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float wj = ej[j] * __expf(mj[j] - nm);  // 0 past the last partition
+                    den += wj;
+                    acc.x += wj * xj[j].x; acc.y += wj * xj[j].y;
+                    acc.z += wj * xj[j].z; acc.w += wj * xj[j].w;
+                }
+                mx = nm;
             }
-            for (; s2 < parts; ++s2) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (size_t)s2 * D));
-                const float wj = wh[s2];
-                acc4[0].x += wj * x.x; acc4[0].y += wj * x.y;
-                acc4[0].z += wj * x.z; acc4[0].w += wj * x.w;
-            }
-            const float4 a = make_float4(acc4[0].x + acc4[1].x, acc4[0].y + acc4[1].y,
-                                         acc4[0].z + acc4[1].z, acc4[0].w + acc4[1].w);
-            const float4 c = make_float4(acc4[2].x + acc4[3].x, acc4[2].y + acc4[3].y,
-                                         acc4[2].z + acc4[3].z, acc4[2].w + acc4[3].w);
-            const float inv = 1.f / dens[h];
+            const float inv = 1.f / den;
             T* out = reinterpret_cast<T*>(p.out) + (qh0 + h) * D + d;
-            const uint32_t lo = M::pack((a.x + c.x) * inv, (a.y + c.y) * inv);
-            const uint32_t hi = M::pack((a.z + c.z) * inv, (a.w + c.w) * inv);
+            const uint32_t lo = M::pack(acc.x * inv, acc.y * inv);
+            const uint32_t hi = M::pack(acc.z * inv, acc.w * inv);
             *reinterpret_cast<uint2*>(out) = make_uint2(lo, hi);
         }
         if (tid == 0) *counter = 0;                        // ready for the next step
