@@ -555,10 +555,19 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
                         p.rec_l[rec * G + hB] = ts.lB * ex2(ts.mB - ts.tB);
                     }
                 }
-                __threadfence();
+                // the warp sync orders the lanes' record writes before lane 0's
+                // acq_rel add (release); the add that completes the segment
+                // acquires every other piece's records for this warp
                 __syncwarp();
                 int last = 0;
-                if (lane == 0) last = atomicAdd(p.counters + z, 1) == (int)(wlast - wfirst);
+                if (lane == 0) {
+                    int before;
+                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                                 : "=r"(before)
+                                 : "l"(p.counters + z)
+                                 : "memory");
+                    last = before == (int)(wlast - wfirst);
+                }
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     // the merge waits for the end of the range, when the
@@ -574,7 +583,7 @@ __global__ void __launch_bounds__(kDecodeThreads, kFp8 ? kMinCtasPerSmFp8 : kMin
         }
         cur.advance(1, p, B, Hkv, max_ctx);
     }
-    __threadfence();
+    __syncwarp();
     for (int i = 0; i < 2; ++i) {
         const int4 e = pend[i];
         if (e.x < 0) continue;
