@@ -389,10 +389,9 @@ int pa_decode_static_workspace(const void* q, const void* k_cache, const void* v
  * counters, int32 [num_seqs][num_kv_heads], which must be zero on entry and
  * are zero again when the step has run (set them to zero once after
  * allocation; after a PA_DEVERR_WAIT_TIMEOUT, zero them again).  The merge
- * stages its weights in shared memory: (Hq/Hkv) * (max_num_partitions + 1)
- * must not exceed 2096 at head_dim 128 or 1072 at head_dim 64, else
- * PA_ERR_UNSUPPORTED.  out [B][Hq][D] receives the
- * attention output.  k_cache, v_cache and the workspace are device memory;
+ * reads the partition records four at a time from global memory, so any
+ * partition count pa_decode_split accepts works.  out [B][Hq][D] receives
+ * the attention output.  k_cache, v_cache and the workspace are device memory;
  * q, k, v, slot_mapping, block_tables, context_lens and out may be device
  * memory or pinned host memory that the device reaches through unified
  * addressing (each CTA reads its inputs and writes its output directly, so

@@ -381,9 +381,6 @@ int decode_step(const void* q, const void* k, const void* v, const int64_t* slot
     if (!aligned16(tmp_out) || !aligned16(max_logits) || !aligned16(exp_sums) ||
         (reinterpret_cast<uintptr_t>(counters) & 3u))
         return PA_ERR_INVALID_ARG;
-    const int G = shp->num_q_heads / shp->num_kv_heads;
-    if ((int64_t)G * max_num_partitions + G > pa::decode_merge_floats(shp->head_dim))
-        return PA_ERR_UNSUPPORTED;
     CUtensorMap tmk, tmv;
     if ((st = encode_cache_map(&tmk, k_cache, shp, ck.fp8)) != PA_OK) return st;
     if ((st = encode_cache_map(&tmv, v_cache, shp, ck.fp8)) != PA_OK) return st;

@@ -163,8 +163,6 @@ cudaError_t launch_reshape_and_cache_fp8(int dtype, const void* k, const void* v
                                          int64_t num_tokens, int64_t num_slots, int row_elems,
                                          float k_scale, float v_scale, int* err,
                                          cudaStream_t stream);
-// Float capacity of the decode kernel's merge area (bounds G * S in the fused step).
-int decode_merge_floats(int head_dim);
 cudaError_t launch_reduce(int dtype, int head_dim, const ReduceParams& p, int num_seqs,
                           cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, const int64_t* slots,

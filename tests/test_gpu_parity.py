@@ -234,3 +234,14 @@ def test_fused_step_back_to_back_steps(dev):
         assert_close(out.float().cpu().numpy(), want, f"fused step {step}")
         assert int(ws[3].abs().sum()) == 0
     assert lib.read_device_errors(dev) == 0
+
+
+def test_fused_step_with_hundreds_of_partitions(dev):
+    """The fused step's merge reads the partition records four at a time, so
+    any partition count works: 500 16-token partitions of an 8,000-token
+    context at G = 8 (with contexts of 4,001 and 17 tokens beside it), cache
+    write and output against the oracle."""
+    w = pin.build_workload(params=dict(dtype="bf16", num_seqs=3, lens=[8000, 4001, 17],
+                                       num_q_heads=64, num_kv_heads=8, head_dim=128,
+                                       block_size=16), seed=91)
+    check_workload(w, dev, modes=("fused",), partition_size=16)
