@@ -364,13 +364,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (j == 0 || need) m = mx;                     // key 0 is visible to every row
             // P = 2^(x scale log2(e) - m) in registers (before the previous
             // product has finished)
+            // two keys per step in packed fp32 (x sl - m, p - hi and the row
+            // sums each one instruction for the pair)
             uint32_t hi[kTcRowKeys / 2], lo[kTcRowKeys / 2];
-            float ps[8];
+            uint64_t ps[4];                                  // partial sums, two lanes each
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ps[e] = 0.f;
+            for (int e = 0; e < 4; ++e) ps[e] = 0ull;
+            const uint64_t sl2 = f32x2_pack(sl, sl), negm2 = f32x2_pack(-m, -m);
+            const uint64_t minus1 = f32x2_pack(-1.f, -1.f);
 #pragma unroll
             for (int e = 0; e < kTcRowKeys / 2; ++e) {
-                const float p0 = ex2(fmaf(x[2 * e], sl, -m)), p1 = ex2(fmaf(x[2 * e + 1], sl, -m));
+                float a0, a1;
+                f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * e], x[2 * e + 1]), sl2, negm2), a0, a1);
+                const float p0 = ex2(a0), p1 = ex2(a1);
                 if (kSplitP) {
                     // bf16 hi = p with its low 16 bits cut off (exact in fp32), lo =
                     // the remainder, also cut to bf16: hi + lo carries p to 2^-15,
@@ -378,16 +384,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const float h0 = __uint_as_float(__float_as_uint(p0) & 0xffff0000u);
                     const float h1 = __uint_as_float(__float_as_uint(p1) & 0xffff0000u);
                     hi[e] = prmt(__float_as_uint(p0), __float_as_uint(p1), 0x7632u);
-                    lo[e] = prmt(__float_as_uint(p0 - h0), __float_as_uint(p1 - h1), 0x7632u);
-                    ps[e & 7] += p0 + p1;
+                    const uint64_t pp = f32x2_pack(p0, p1);
+                    float d0, d1;
+                    f32x2_unpack(f32x2_fma(f32x2_pack(h0, h1), minus1, pp), d0, d1);
+                    lo[e] = prmt(__float_as_uint(d0), __float_as_uint(d1), 0x7632u);
+                    ps[e & 3] = f32x2_add(ps[e & 3], pp);
                 } else {
                     hi[e] = M::pack(p0, p1);
                     const float2 u = M::unpack(hi[e]);
                     lo[e] = 0u;
-                    ps[e & 7] += u.x + u.y;
+                    ps[e & 3] = f32x2_add(ps[e & 3], f32x2_pack(u.x, u.y));
                 }
             }
-            l = l * f + (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7])));
+            float q8[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f32x2_unpack(ps[e], q8[2 * e], q8[2 * e + 1]);
+            l = l * f + (((q8[0] + q8[1]) + (q8[2] + q8[3])) + ((q8[4] + q8[5]) + (q8[6] + q8[7])));
             // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
             if (j > 0) {
                 wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1);
