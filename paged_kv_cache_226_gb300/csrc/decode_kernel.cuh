@@ -5,11 +5,12 @@
 // table and gathers K and V while it computes (ta-paperlens "LLM serving
 // from scratch", section on fragmentation and PagedAttention).
 //
-// Data movement: a producer warp reads the block table and issues one TMA
-// box per 16-token half-row tile ([16 tokens][64 dims] of one KV head, 128 B
-// rows, 128 B swizzle) into an 8-stage shared-memory ring guarded by
-// mbarriers; a block of 32 tokens is two tiles.  The consumer warps (two by
-// default, with a 4-stage ring and six CTAs per SM) take the tiles round robin.
+// Data movement: a producer warp reads the block table and issues the TMA
+// boxes of each 16-token tile ([16 tokens][64 dims] of one KV head per box,
+// 128 B rows, 128 B swizzle; K then V) into a shared-memory ring guarded by
+// mbarriers (4 stages of 8 KiB, 8 of 4 KiB for an FP8 cache), two tiles per
+// round with one lane per box; a block of 32 tokens is two tiles.  The two
+// consumer warps take the tiles round robin (FP8: in pairs); six CTAs per SM.
 //
 // Math per tile and warp (the G <= 8 query heads of the group are the N = 8
 // columns of two m16n8k16 tile products; columns >= G are zero):
@@ -23,7 +24,9 @@
 //   accumulates the rounded values), for bf16 as a hi + lo pair of bf16
 //   values whose sum carries P to ~2^-17 -- transposed in registers with
 //   movmatrix, and O^T[d][h] += V^T[d][:] . P^T[:][h] with fp32 accumulation.
-// The four warps' (m, l, O) are merged through shared memory at the end.
+// The consumer warps' (m, l, O) are merged through shared memory at the end;
+// a partitioned CTA writes a record, and in the fused step the last one of
+// a (sequence, KV head) merges the records.
 #pragma once
 
 #include "decode_tile.cuh"
