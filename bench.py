@@ -95,16 +95,19 @@ def source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config: str, kernel: str):
+def profiled_traffic(config: str, kernel: str, partition=None):
     """DRAM bytes per launch from a committed ncu summary
     (profiles/<kernel>_<config>.json), if it was taken on the kernel's current
-    sources; else None."""
+    sources and, for a partitioned launch, at the same partition size; else
+    None."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         p = json.load(f)
     if p.get("source_sha256_16") != source_hash(kernel):
+        return None
+    if partition is not None and p.get("partition_tokens") != partition:
         return None
     return p.get("dram_bytes_per_launch")
 
@@ -448,7 +451,9 @@ def decode_summary(w: pin.Workload, mode: str, partition: int, kv_dtype: str, nb
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "algorithmic_bytes_per_launch": dom_bytes,
-                     "traffic": profiled_traffic(traffic_key, dom)},
+                     "traffic": profiled_traffic(
+                         traffic_key, dom,
+                         partition if dom in ("paged_decode_step", "paged_decode_split") else None)},
         "clocks": tm["clocks"],
         "gpu_launches": LAUNCHES_PER_STEP[mode] * len(tm["step_ms"]),
     }
@@ -486,7 +491,7 @@ def bench_sub_configs(names, args, dev, stream, flush, hbm, peak_src):
             w = pin.build_workload(cfg, seed=rank_seed(cfg, 0), pool_device=dev)
             max_len = int(w.context_lens.max())
             p = partition or lib.choose_partition(w.num_seqs, w.num_kv_heads, max_len,
-                                                  w.block_size, dev)
+                                                  w.block_size, dev, w.context_lens)
             d, plan, nb = decode_setup(w, dev, mode, p, kv_dtype, rank_seed(cfg, 0) + 7)
             tm = time_steps(plan, flush, dev, stream, args.steps, args.warmup, dev.index or 0, 1)
             res = decode_summary(w, mode, p, kv_dtype, nb, tm, dev, 1, hbm, peak_src,
@@ -517,7 +522,7 @@ def bench_ours(args):
     max_len = int(w.context_lens.max())
     mode = args.mode if args.mode != "auto" else "fused"
     partition = args.partition or lib.choose_partition(w.num_seqs, w.num_kv_heads, max_len,
-                                                       w.block_size, dev)
+                                                       w.block_size, dev, w.context_lens)
     d, plan, nb = decode_setup(w, dev, mode, partition, args.kv_dtype,
                                rank_seed(args.config, rank) + 7)
     flush = L2Flush(dev)

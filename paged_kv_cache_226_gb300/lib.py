@@ -606,17 +606,27 @@ CTAS_PER_SM = 6          # resident decode CTAs per SM in the shipped build
 
 
 def choose_partition(num_seqs: int, num_kv_heads: int, max_context_len: int,
-                     block_size: int = 16, device=None) -> int:
+                     block_size: int = 16, device=None, context_lens=None) -> int:
     """Partition size for the split / fused paths.
 
     With at least half as many (sequence, KV head) pairs as resident CTA
     slots, the pairs alone give every slot work: 1024-token partitions then
     leave most contexts of a ragged batch in one partition (no merge) and
-    the rest in few (measured on the fused step: shared-prefix batch 124 us
-    against 139 us at 512 tokens, Llama-3-8B-shaped batch equal).  Fewer
-    pairs (long contexts, small batches) get about one partition per slot,
-    so the per-partition start-up cost is paid fewer times:
-    round_up(max_len * pairs / slots, 512), clamped to [512, 4096]."""
+    the rest in few (measured on the fused step: shared-prefix batch 119 us
+    against 133 us at 512 tokens, Llama-3-8B-shaped batch 60 us against 62).
+
+    Fewer pairs (long contexts, small batches): the smallest multiple of 512
+    that cuts the batch into at most 4.8 CTAs per SM, counting every
+    context's ragged last piece (``context_lens``, host values; without them
+    every context is taken at ``max_context_len``).  Fewer CTAs pay the
+    per-partition start and merge fewer times, but below ~3 per SM too few
+    stages are in flight to keep HBM busy; more than one wave of CTAs
+    leaves a tail of late, long partitions.  Measured on the fused step
+    (µs per layer-step, best partition, this rule's choice): 256 pairs of
+    4096 tokens 91.8 at 2048 (2048; 1536 gives 94.3); 64 pairs of
+    U[32768, 50000] 217.2 at 4352 (4096: 220.1; 3584 gives 230.3);
+    32 x U[128, 4096] x 8 heads 54.9 at 1024 (1024; 2048 gives 67.4);
+    40 x 4096 x 8 heads 108.3 at 2048 (2048; 1536 gives 115.5)."""
     if device is None and torch.cuda.is_available():
         device = torch.cuda.current_device()
     sms = torch.cuda.get_device_properties(device).multi_processor_count if device is not None \
@@ -628,8 +638,27 @@ def choose_partition(num_seqs: int, num_kv_heads: int, max_context_len: int,
     elif 2 * pairs >= slots:
         p = 1024
     else:
-        p = -(-max_context_len * pairs // slots)
-        p = min(4096, max(512, -(-p // 512) * 512))
+        if context_lens is None:
+            lens = np.full(max(1, num_seqs), max_context_len, dtype=np.int64)
+        else:
+            if isinstance(context_lens, torch.Tensor):
+                context_lens = context_lens.detach().cpu().numpy()
+            lens = np.asarray(context_lens, dtype=np.int64).reshape(-1)
+        limit = (24 * sms) // 5                        # 4.8 CTAs per SM
+
+        def ctas(units: int) -> int:                   # CTAs at 512 * units tokens
+            return num_kv_heads * int(np.sum(-(-lens // (512 * units))))
+
+        # The count falls as the partition grows; one partition per context
+        # (pairs < slots / 2 <= limit CTAs) always fits.
+        lo, hi = 1, max(1, -(-max_context_len // 512))
+        while lo < hi:
+            mid = (lo + hi) // 2
+            if ctas(mid) <= limit:
+                hi = mid
+            else:
+                lo = mid + 1
+        p = 512 * lo
     return max(block_size, p - p % block_size)
 
 
@@ -723,11 +752,16 @@ class StepPlan:
     addressing, with no copy launch (on a Grace-Blackwell node the fastest
     way to move a step's inputs in and its output out).  The caches and the
     workspace stay in device memory.
+
+    ``partition_size=None`` takes ``choose_partition`` for the batch: with
+    the lengths counted when ``context_lens`` is in host memory, else every
+    context taken at ``max_context_len`` (no device read).  Any multiple of
+    the block size gives the same result; the size only sets the speed.
     """
 
     def __init__(self, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
                  context_lens, scale: float, max_context_len: int, out=None,
-                 mode: str = "auto", partition_size: int = DEFAULT_PARTITION, workspace=None,
+                 mode: str = "auto", partition_size: Optional[int] = None, workspace=None,
                  k_scale: Optional[float] = None, v_scale: Optional[float] = None):
         self._lib = load()
         self.fp8 = k_cache.dtype == torch.uint8
@@ -756,6 +790,10 @@ class StepPlan:
         if mode in ("fused", "balanced") and T != q.shape[0]:
             raise ValueError("the fused step takes exactly one new token per sequence")
         self.mode = mode
+        if partition_size is None:
+            partition_size = choose_partition(
+                q.shape[0], k_cache.shape[2], max_context_len, k_cache.shape[1], dev,
+                context_lens if context_lens.device.type == "cpu" else None)
         self.partition_size = int(partition_size)
         self.num_partitions = num_partitions(max_context_len, partition_size)
         self._shape = shp

@@ -89,19 +89,57 @@ def test_profiled_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench.profiled_traffic("absent", "paged_prefill") is None
 
 
+def test_profiled_traffic_follows_the_partition_size(tmp_path, monkeypatch):
+    """A partitioned launch's figure is reported only at the partition size
+    it was captured with."""
+    import json
+    import bench
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = {"source_sha256_16": bench.source_hash("paged_decode_step"), "partition_tokens": 2048,
+           "dram_bytes_per_launch": 99}
+    (prof / "paged_decode_step_w.json").write_text(json.dumps(rec))
+    assert bench.profiled_traffic("w", "paged_decode_step", 2048) == 99
+    assert bench.profiled_traffic("w", "paged_decode_step", 1536) is None
+    del rec["partition_tokens"]
+    (prof / "paged_decode_step_w.json").write_text(json.dumps(rec))
+    assert bench.profiled_traffic("w", "paged_decode_step", 2048) is None
+
+
 def test_choose_partition_rule():
     """The partition size rule on a 152-SM part with six decode CTAs per SM
     (912 slots): many (sequence, KV head) pairs get 1024-token partitions,
-    few pairs about one partition per slot (a multiple of 512, at most 4096),
-    short contexts 512."""
+    few pairs the smallest multiple of 512 giving at most 729 CTAs (4.8 per
+    SM) with each context's last piece counted, short contexts 512."""
     from paged_kv_cache_226_gb300 import lib
     if __import__("torch").cuda.is_available():
         pytest.skip("the rule is checked here for the 152-SM default only")
     assert lib.choose_partition(64, 8, 2048) == 1024            # 512 pairs
     assert lib.choose_partition(256, 8, 4608) == 1024           # shared-prefix batch
-    assert lib.choose_partition(32, 8, 4096) == 1536            # 256 pairs: ceil(1150 / 512)
-    assert lib.choose_partition(8, 8, 50000) == 3584            # 64 pairs: ceil(3509 / 512)
-    assert lib.choose_partition(1, 1, 10 ** 6) == 1536          # ceil(1097 / 512)
-    assert lib.choose_partition(1, 1, 10 ** 7) == 4096          # clamped
+    assert lib.choose_partition(32, 8, 4096) == 2048            # 1536: 768 CTAs; 2048: 512
+    assert lib.choose_partition(8, 8, 50000) == 4608            # 64 x ceil(50000 / 4608) = 704
+    assert lib.choose_partition(8, 8, 45056) == 4096            # 64 x 11 = 704; 3584: 64 x 13
+    assert lib.choose_partition(1, 1, 10 ** 6) == 1536          # 652 pieces; 1024: 977
+    assert lib.choose_partition(1, 1, 10 ** 7) == 13824         # 724 pieces; 13312: 752
     assert lib.choose_partition(4, 2, 250) == 512               # short contexts
     assert lib.choose_partition(64, 8, 2048, block_size=32) % 32 == 0
+
+
+def test_choose_partition_counts_ragged_contexts():
+    """With the context lengths given, the short contexts' single pieces are
+    counted as such: one 49152-token context and seven of 1024 tokens, 8 KV
+    heads, fit 729 CTAs at 1024 tokens (8 x (48 + 7) = 440), while taking
+    every context at the maximum needs 4608 (8 x 8 x 11 = 704)."""
+    import numpy as np
+    import torch
+    from paged_kv_cache_226_gb300 import lib
+    if torch.cuda.is_available():
+        pytest.skip("the rule is checked here for the 152-SM default only")
+    lens = [49152] + [1024] * 7
+    assert lib.choose_partition(8, 8, 49152) == 4608
+    assert lib.choose_partition(8, 8, 49152, context_lens=lens) == 1024
+    assert lib.choose_partition(8, 8, 49152, context_lens=np.asarray(lens, np.int32)) == 1024
+    assert lib.choose_partition(8, 8, 49152, context_lens=torch.tensor(lens)) == 1024
+    # empty contexts add no CTAs: 8 x 48 = 384 at 1024 tokens, 8 x 96 = 768 > 729 at 512
+    assert lib.choose_partition(8, 8, 49152, context_lens=[0] * 7 + [49152]) == 1024

@@ -171,6 +171,35 @@ def test_step_plan_eager_and_graph_replay(dev, mode):
     assert lib.read_device_errors(dev) == 0
 
 
+def test_step_plan_chooses_the_partition(dev):
+    """Without partition_size the plan takes the partition rule: over the
+    lengths when context_lens is pinned host memory, with every context at
+    the maximum when it is on the device.  One 12288-token context and
+    seven of 256 tokens over 8 KV heads give different sizes (1536 at the
+    maximum, 512 counted); both match the reference."""
+    lens = [12288] + [256] * 7
+    w = pin.build_workload(params=dict(dtype="fp16", num_seqs=8, lens=lens, num_q_heads=32,
+                                       num_kv_heads=8, head_dim=128, block_size=16), seed=41)
+    d = to_device(w, dev)
+    kc, vc, _ = oracle.reshape_and_cache(pin.bits(w.k_new), pin.bits(w.v_new), w.slot_mapping,
+                                         pin.bits(w.k_cache), pin.bits(w.v_cache), w.block_size)
+    want = oracle.paged_decode(pin.bits(w.q), kc, vc, w.block_tables, w.context_lens, w.scale,
+                               w.dtype)
+    at_max = lib.choose_partition(8, 8, 12288, 16, dev)
+    counted = lib.choose_partition(8, 8, 12288, 16, dev, w.context_lens)
+    assert at_max != counted
+    host_lens = d["context_lens"].cpu().pin_memory()
+    for lens_t, expect in ((d["context_lens"], at_max), (host_lens, counted)):
+        plan = lib.StepPlan(d["q"], d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"],
+                            d["v_cache"], d["block_tables"], lens_t, w.scale, 12288,
+                            mode="fused")
+        assert plan.partition_size == expect
+        got = plan()
+        torch.cuda.synchronize(dev)
+        assert_close(got.float().cpu().numpy(), want, f"partition {expect}")
+    assert lib.read_device_errors(dev) == 0
+
+
 def test_fused_step_rejects_a_slot_that_is_not_the_last_position(dev):
     """A slot other than position L-1's is not written; attention runs on the
     cache as it was, and the device error word reports it."""
