@@ -9,9 +9,9 @@
 // that KV head, so every K/V tile is read once for all of them.
 //
 // Per 128-key tile j (keys 128 j .. 128 j + 127 through the block table):
-//   S_j = Q K_j^T          128 x 128 x 128 into tensor memory (two buffers),
-//                          Q from tensor memory (stored there once), K from
-//                          its TMA-staged tile in shared memory
+//   S_j = Q K_j^T          128 x 128 x 128 into tensor memory (three
+//                          buffers), Q from shared memory (stored there once,
+//                          laid out like a K tile), K from its TMA-staged tile
 //   P_j = 2^(S_j - m)      eight softmax warps, two threads per row (64
 //                          keys each, row maxima and sums exchanged through
 //                          shared memory), a lazily raised running max m (log2
@@ -23,16 +23,19 @@
 //   O  += P_j V_j          128 x 128 x 128, P read from tensor memory, V from
 //                          its TMA-staged [key][dim] tile (MN-major), O in
 //                          tensor memory
-// Warp roles: warp 0 streams K tiles and warp 10 V tiles (three stages each,
-// in the shared memory Q does not need) with TMA, 16-token boxes of the paged
+// Warp roles: warp 0 streams K tiles and warp 10 V tiles (three and two
+// stages beside Q in shared memory) with TMA, 16-token boxes of the paged
 // cache, each at its own pace; lane 0 of warp 1 issues the S products and
 // lane 0 of warp 11 the P V products, committing them to mbarriers; warps
 // 2-9 run the softmax and the epilogue.  One control warp sits on each of
 // the SM's four schedulers: a thread issuing MMAs beside warps with ALU work
 // ready is starved of issue slots, and two issuers halve what each must get
-// through.  S_{j+1} is issued before P_j is ready, and P_j is computed before
-// P_{j-1} V_{j-1} has finished, so only the store of P waits on the previous
-// product; S_{j+2} overwrites P_j, so its issuer waits for P_j V_j first.
+// through.  S_{j+1} and S_{j+2} are issued before P_j is ready, and P_j is
+// computed and stored before P_{j-1} V_{j-1} has finished (only a rescale of O
+// waits for that product); S_{j+3} overwrites P_j, so its issuer waits for
+// P_j V_j first.  The P-ready barrier is kept per buffer too: the softmax may
+// run two tiles ahead of the P V issuer, and one barrier would let its phases
+// pass the issuer's parity check.
 // Every mbarrier wait gives up after 1 s and flags PA_DEVERR_WAIT_TIMEOUT;
 // the softmax warps then run their remaining iterations without waiting (so
 // their barriers always complete), and tensor memory is always released.
@@ -50,7 +53,8 @@ namespace pa {
 constexpr int kTcRows = 128;                 // query rows per CTA (tokens x heads)
 constexpr int kTcKeys = 128;                 // keys per K/V tile
 constexpr int kTcKStages = 3;                // K tiles in flight (free once S is computed)
-constexpr int kTcVStages = 3;                // V tiles in flight (held until P V is done)
+constexpr int kTcVStages = 2;                // V tiles in flight (held until P V is done)
+constexpr int kTcSBufs = 3;                  // S / P buffers in tensor memory
 // softmax threads per query row: two (64 keys each, eight softmax warps)
 // measured 3 % faster than four, with fewer ALU-ready warps beside the MMA
 // issuers on each scheduler
@@ -64,12 +68,13 @@ constexpr int kTcSoftmaxWarps = 4 * kTcPerRow;
 constexpr int kTcVWarp = 2 + kTcSoftmaxWarps;  // the V producer, after the softmax warps
 constexpr int kTcPvWarp = 3 + kTcSoftmaxWarps; // issues P V (warp 1 issues S)
 constexpr int kTcThreads = (4 + kTcSoftmaxWarps) * 32;
-constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0/P0, S1/P1, O, Q
+constexpr uint32_t kTcCols = 512;            // tensor-memory columns: S0/P0, S1/P1, S2/P2, O
 constexpr int kTcOperand = 32768;            // 128 rows x 2 halves x 128 B
 constexpr int kTcHalf = 16384;               // one 64-element half: 128 rows x 128 B
 
 struct TcLayout {
-    static constexpr int kK = 0;
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTcOperand;
     static constexpr int kV = kK + kTcKStages * kTcOperand;
     static constexpr int kBytes = kV + kTcVStages * kTcOperand;
     static constexpr int kDynamicSmem = kBytes + 1024;
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t k_full[kTcKStages], k_empty[kTcKStages];
     __shared__ __align__(8) uint64_t v_full[kTcVStages], v_empty[kTcVStages];
     __shared__ float xchg[3][kTcPerRow][kTcRows];   // row maxima (two sets by tile parity), sums
-    __shared__ __align__(8) uint64_t s_full[2], q_full, p_full, o_done[2];
+    __shared__ __align__(8) uint64_t s_full[kTcSBufs], q_full, p_full[kTcSBufs], o_done[kTcSBufs];
     __shared__ uint32_t tmem_base;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -185,10 +190,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
+        for (int i = 0; i < kTcSBufs; ++i) mbar_init(&s_full[i], 1);
         mbar_init(&q_full, kTcSoftmaxWarps);                // one arrival per softmax warp
-        mbar_init(&p_full, kTcSoftmaxWarps);
-        for (int i = 0; i < 2; ++i) mbar_init(&o_done[i], 1);
+        for (int i = 0; i < kTcSBufs; ++i) mbar_init(&p_full[i], kTcSoftmaxWarps);
+        for (int i = 0; i < kTcSBufs; ++i) mbar_init(&o_done[i], 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
@@ -211,13 +216,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_base;
-    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO = tmem + 256;
-    const uint32_t tQ = tmem + 384;                         // Q: dims 2c, 2c+1 in column c
+    const uint32_t tO = tmem + 128 * kTcSBufs;             // S_j / P_j in columns 128 (j % 3)
 
     if (warp == 0 || warp == kTcVWarp) {
         // ------------------------------------------------------------------
-        // producers: K tiles (warp 0, free once S is computed) and V tiles
-        // (warp 10, held until P V is done), three stages each
+        // producers: K tiles (warp 0, free once S is computed, three stages)
+        // and V tiles (warp 10, held until P V is done, two stages)
         // ------------------------------------------------------------------
         if (lane == 0) prefetch_tensor_map(warp == 0 ? &tmap_k : &tmap_v);
         // warp 0 streams K, warp 10 V, each at its own pace (issuing the
@@ -231,8 +235,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == 1 || warp == kTcPvWarp) {
         // ------------------------------------------------------------------
         // MMA issuers, one thread each on two schedulers: warp 1 issues S_j,
-        // the last warp P_j V_j.  S_j overwrites P_{j-2}, so it waits for that
-        // product (o_done by tile parity); P V in order accumulates O.
+        // the last warp P_j V_j.  S_j overwrites P_{j-3}, so it waits for that
+        // product (o_done of buffer j % 3); P V in order accumulates O.
         // ------------------------------------------------------------------
         if (lane == 0) {
             constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, kBf16, false);
@@ -241,32 +245,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (warp == 1) {
                 ok = mbar_wait(&q_full, 0);
                 tc_fence_after_sync();
+                const uint32_t aQ = smem_u32(smem + Lay::kQ);
                 for (int j = 0; j < n_tiles && ok; ++j) {
-                    const int s = j % kTcKStages, bb = j & 1;
+                    const int s = j % kTcKStages, sb = j % kTcSBufs;
                     ok = mbar_wait(&k_full[s], (j / kTcKStages) & 1);
-                    if (ok && j >= 2) ok = mbar_wait(&o_done[bb], ((j - 2) >> 1) & 1);
+                    if (ok && j >= kTcSBufs) ok = mbar_wait(&o_done[sb], (j / kTcSBufs - 1) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t aK = smem_u32(smem + Lay::kK + s * kTcOperand);
-                    const uint32_t dS = bb ? tS1 : tS0;
+                    const uint32_t dS = tmem + 128 * sb;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * kTcHalf + (kk & 3) * 32;
-                        mma_f16_ts(dS, tQ + 8 * kk, smem_desc_sw128(aK + off, 16, 1024), kIdS,
-                                   kk > 0);
+                        mma_f16_ss(dS, smem_desc_sw128(aQ + off, 16, 1024),
+                                   smem_desc_sw128(aK + off, 16, 1024), kIdS, kk > 0);
                     }
-                    mma_commit(&s_full[bb]);
+                    mma_commit(&s_full[sb]);
                     mma_commit(&k_empty[s]);                // S_j has read K_j
                 }
             } else {
                 for (int j = 0; j < n_tiles && ok; ++j) {
                     const int s = j % kTcVStages;
-                    ok = mbar_wait(&p_full, j & 1);
+                    ok = mbar_wait(&p_full[j % kTcSBufs], (j / kTcSBufs) & 1);
                     if (ok) ok = mbar_wait(&v_full[s], (j / kTcVStages) & 1);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t aV = smem_u32(smem + Lay::kV + s * kTcOperand);
-                    const uint32_t tP = (j & 1) ? tS1 : tS0;    // P_j over S_j
+                    const uint32_t tP = tmem + 128 * (j % kTcSBufs);   // P_j over S_j
 #pragma unroll
                     for (int part = 0; part < (kSplitP ? 2 : 1); ++part) {
 #pragma unroll
@@ -275,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                        smem_desc_sw128(aV + kk * 16 * 128, kTcHalf, 1024), kIdPV,
                                        j > 0 || part > 0 || kk > 0);
                     }
-                    mma_commit(&o_done[j & 1]);
+                    mma_commit(&o_done[j % kTcSBufs]);
                     mma_commit(&v_empty[s]);                // P_j V_j has read V_j
                 }
             }
@@ -294,12 +299,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t my_cols = lane_addr + kTcRowKeys * part;
         const float sl = p.scale_log2;
         float m = -INFINITY, l = 0.f;
-        // this thread's quarter of its Q row into tensor memory: 16 columns
+        // this thread's slice of its Q row into shared memory, laid out like
+        // a K tile (the A operand of S); visible to the tensor cores after the
+        // proxy fence
 #pragma unroll
-        for (int c = 0; c < kTcChunks; ++c)
-            tmem_st16(tQ + lane_addr + (kTcRowKeys / 2) * part + 16 * c,
-                      *reinterpret_cast<const uint32_t(*)[16]>(qw + 16 * c));
-        tmem_wait_st();
+        for (int c = 0; c < kTcRowVec; ++c)
+            *reinterpret_cast<uint4*>(smem + Lay::kQ + tc_chunk(r, kTcRowVec * part + c)) =
+                make_uint4(qw[4 * c], qw[4 * c + 1], qw[4 * c + 2], qw[4 * c + 3]);
+        fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_full);
@@ -317,15 +324,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             return make_float4(xchg[set][0][r], xchg[set][1][r], xchg[set][2][r], xchg[set][3][r]);
         };
         for (int j = 0; j < n_tiles; ++j) {
-            const int bb = j & 1, s = j % kTcVStages;
-            wait(&s_full[bb], (j >> 1) & 1);
+            const int bb = j & 1, s = j % kTcVStages, sb = j % kTcSBufs;
+            const uint32_t tS = tmem + 128 * sb;            // S_j, then P_j
+            wait(&s_full[sb], (j / kTcSBufs) & 1);
             tc_fence_after_sync();
             float x[kTcRowKeys];
             {
                 uint32_t v0[kTcRowKeys];
 #pragma unroll
                 for (int c = 0; c < kTcChunks; ++c)
-                    tmem_ld32((bb ? tS1 : tS0) + my_cols + 32 * c,
+                    tmem_ld32(tS + my_cols + 32 * c,
                               *reinterpret_cast<uint32_t(*)[32]>(v0 + 32 * c));
                 tmem_wait_ld();
 #pragma unroll
@@ -400,12 +408,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) f32x2_unpack(ps[e], q8[2 * e], q8[2 * e + 1]);
             l = l * f + (((q8[0] + q8[1]) + (q8[2] + q8[3])) + ((q8[4] + q8[5]) + (q8[6] + q8[7])));
-            // P_{j-1} V_{j-1} must be complete before O is rescaled or P rewritten
-            if (j > 0) {
-                wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1);
+            // P_{j-1} V_{j-1} must be complete before O is rescaled
+            const bool rescale = __any_sync(0xffffffffu, need);
+            if (j > 0 && rescale) {
+                wait(&o_done[(j - 1) % kTcSBufs], ((j - 1) / kTcSBufs) & 1);
                 tc_fence_after_sync();
             }
-            if (__any_sync(0xffffffffu, need)) {
+            if (rescale) {
 #pragma unroll
                 for (int c = 0; c < kTcChunks; ++c) {
                     uint32_t v[32];
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // P into tensor memory over S_j, the A operand of P V: keys 2c,
             // 2c+1 in column c of [0, 64) (bf16: lo parts in [64, 128)); this
             // thread's 32 keys are 16 columns at 16 part
-            const uint32_t tP = bb ? tS1 : tS0;
+            const uint32_t tP = tS;
 #pragma unroll
             for (int c = 0; c < kTcChunks; ++c) {
                 const uint32_t col = lane_addr + (kTcRowKeys / 2) * part + 16 * c;
@@ -441,10 +450,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             fence_proxy_async_smem();                       // the cleared V rows
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full);
+            if (lane == 0) mbar_arrive(&p_full[sb]);
         }
         // epilogue: O / l for the chunk's rows, l summed over the row's threads
-        wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1);
+        wait(&o_done[(n_tiles - 1) % kTcSBufs], ((n_tiles - 1) / kTcSBufs) & 1);
         tc_fence_after_sync();
         const float4 l4 = exchange(2, l);
         if (!failed) {
