@@ -370,39 +370,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool need = j > 0 && mx > m + kRescaleThresholdLog2;
             const float f = need ? ex2(m - mx) : 1.f;
             if (j == 0 || need) m = mx;                     // key 0 is visible to every row
-            // P = 2^(x scale log2(e) - m) in registers (before the previous
-            // product has finished)
-            // two keys per step in packed fp32 (x sl - m, p - hi and the row
-            // sums each one instruction for the pair)
-            uint32_t hi[kTcRowKeys / 2], lo[kTcRowKeys / 2];
+            // P = 2^(x scale log2(e) - m), computed and stored into tensor
+            // memory over S_j one 32-key chunk at a time (the A operand of P V:
+            // keys 2i, 2i+1 in column i of [0, 64), bf16 lo parts in [64, 128);
+            // this thread's 64 keys are 32 columns at 32 part), before the
+            // previous product has finished; two keys per step in packed fp32
+            // (x sl - m, p - hi and the row sums each one instruction for the pair)
             uint64_t ps[4];                                  // partial sums, two lanes each
 #pragma unroll
             for (int e = 0; e < 4; ++e) ps[e] = 0ull;
             const uint64_t sl2 = f32x2_pack(sl, sl), negm2 = f32x2_pack(-m, -m);
             const uint64_t minus1 = f32x2_pack(-1.f, -1.f);
 #pragma unroll
-            for (int e = 0; e < kTcRowKeys / 2; ++e) {
-                float a0, a1;
-                f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * e], x[2 * e + 1]), sl2, negm2), a0, a1);
-                const float p0 = ex2(a0), p1 = ex2(a1);
-                if (kSplitP) {
-                    // bf16 hi = p with its low 16 bits cut off (exact in fp32), lo =
-                    // the remainder, also cut to bf16: hi + lo carries p to 2^-15,
-                    // with integer and fp32 adds only
-                    const float h0 = __uint_as_float(__float_as_uint(p0) & 0xffff0000u);
-                    const float h1 = __uint_as_float(__float_as_uint(p1) & 0xffff0000u);
-                    hi[e] = prmt(__float_as_uint(p0), __float_as_uint(p1), 0x7632u);
-                    const uint64_t pp = f32x2_pack(p0, p1);
-                    float d0, d1;
-                    f32x2_unpack(f32x2_fma(f32x2_pack(h0, h1), minus1, pp), d0, d1);
-                    lo[e] = prmt(__float_as_uint(d0), __float_as_uint(d1), 0x7632u);
-                    ps[e & 3] = f32x2_add(ps[e & 3], pp);
-                } else {
-                    hi[e] = M::pack(p0, p1);
-                    const float2 u = M::unpack(hi[e]);
-                    lo[e] = 0u;
-                    ps[e & 3] = f32x2_add(ps[e & 3], f32x2_pack(u.x, u.y));
+            for (int c = 0; c < kTcChunks; ++c) {
+                uint32_t hi[16], lo[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int e = 16 * c + i;
+                    float a0, a1;
+                    f32x2_unpack(f32x2_fma(f32x2_pack(x[2 * e], x[2 * e + 1]), sl2, negm2), a0, a1);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
+                    if (kSplitP) {
+                        // bf16 hi = p with its low 16 bits cut off (exact in fp32),
+                        // lo = the remainder, also cut to bf16: hi + lo carries p to
+                        // 2^-15, with integer and fp32 adds only
+                        const float h0 = __uint_as_float(__float_as_uint(p0) & 0xffff0000u);
+                        const float h1 = __uint_as_float(__float_as_uint(p1) & 0xffff0000u);
+                        hi[i] = prmt(__float_as_uint(p0), __float_as_uint(p1), 0x7632u);
+                        const uint64_t pp = f32x2_pack(p0, p1);
+                        float d0, d1;
+                        f32x2_unpack(f32x2_fma(f32x2_pack(h0, h1), minus1, pp), d0, d1);
+                        lo[i] = prmt(__float_as_uint(d0), __float_as_uint(d1), 0x7632u);
+                        ps[i & 3] = f32x2_add(ps[i & 3], pp);
+                    } else {
+                        hi[i] = M::pack(p0, p1);
+                        const float2 u = M::unpack(hi[i]);
+                        lo[i] = 0u;
+                        ps[i & 3] = f32x2_add(ps[i & 3], f32x2_pack(u.x, u.y));
+                    }
                 }
+                const uint32_t col = lane_addr + (kTcRowKeys / 2) * part + 16 * c;
+                tmem_st16(tS + col, hi);
+                if (kSplitP) tmem_st16(tS + 64 + col, lo);
             }
             float q8[8];
 #pragma unroll
@@ -435,16 +444,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int c = kTcRowVec * part; c < kTcRowVec * (part + 1); ++c)
                         *reinterpret_cast<uint4*>(vd + tc_chunk(r, c)) = make_uint4(0u, 0u, 0u, 0u);
                 }
-            }
-            // P into tensor memory over S_j, the A operand of P V: keys 2c,
-            // 2c+1 in column c of [0, 64) (bf16: lo parts in [64, 128)); this
-            // thread's 32 keys are 16 columns at 16 part
-            const uint32_t tP = tS;
-#pragma unroll
-            for (int c = 0; c < kTcChunks; ++c) {
-                const uint32_t col = lane_addr + (kTcRowKeys / 2) * part + 16 * c;
-                tmem_st16(tP + col, *reinterpret_cast<const uint32_t(*)[16]>(hi + 16 * c));
-                if (kSplitP) tmem_st16(tP + 64 + col, *reinterpret_cast<const uint32_t(*)[16]>(lo + 16 * c));
             }
             tmem_wait_st();
             fence_proxy_async_smem();                       // the cleared V rows
