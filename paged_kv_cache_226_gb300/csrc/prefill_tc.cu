@@ -12,9 +12,8 @@
 //   S_j = Q K_j^T          128 x 128 x 128 into tensor memory (three
 //                          buffers), Q from shared memory (stored there once,
 //                          laid out like a K tile), K from its TMA-staged tile
-//   P_j = 2^(S_j - m)      eight softmax warps, two threads per row (64
-//                          keys each, row maxima and sums exchanged through
-//                          shared memory), a lazily raised running max m (log2
+//   P_j = 2^(S_j - m)      four softmax warps, one thread per row (all 128
+//                          keys of the tile), a lazily raised running max m (log2
 //                          units, threshold 2^8: the accumulator is rescaled
 //                          in tensor memory only when a row's max grows by
 //                          more than that); P goes to tensor memory over S_j
@@ -23,14 +22,14 @@
 //   O  += P_j V_j          128 x 128 x 128, P read from tensor memory, V from
 //                          its TMA-staged [key][dim] tile (MN-major), O in
 //                          tensor memory
-// Warp roles: warp 0 streams K tiles and warp 10 V tiles (three and two
+// Warp roles: warp 0 streams K tiles and warp 6 V tiles (three and two
 // stages beside Q in shared memory) with TMA, 16-token boxes of the paged
 // cache, each at its own pace; lane 0 of warp 1 issues the S products and
-// lane 0 of warp 11 the P V products, committing them to mbarriers; warps
-// 2-9 run the softmax and the epilogue.  One control warp sits on each of
-// the SM's four schedulers: a thread issuing MMAs beside warps with ALU work
-// ready is starved of issue slots, and two issuers halve what each must get
-// through.  S_{j+1} and S_{j+2} are issued before P_j is ready, and P_j is
+// lane 0 of warp 7 the P V products, committing them to mbarriers; warps
+// 2-5 run the softmax and the epilogue.  One control warp and one softmax
+// warp sit on each of the SM's four schedulers: a thread issuing MMAs beside
+// warps with ALU work ready is starved of issue slots, and two issuers halve
+// what each must get through.  S_{j+1} and S_{j+2} are issued before P_j is ready, and P_j is
 // computed and stored before P_{j-1} V_{j-1} has finished (only a rescale of O
 // waits for that product); S_{j+3} overwrites P_j, so its issuer waits for
 // P_j V_j first.  The P-ready barrier is kept per buffer too: the softmax may
@@ -55,14 +54,15 @@ constexpr int kTcKeys = 128;                 // keys per K/V tile
 constexpr int kTcKStages = 3;                // K tiles in flight (free once S is computed)
 constexpr int kTcVStages = 2;                // V tiles in flight (held until P V is done)
 constexpr int kTcSBufs = 3;                  // S / P buffers in tensor memory
-// softmax threads per query row: two (64 keys each, eight softmax warps)
-// measured 3 % faster than four, with fewer ALU-ready warps beside the MMA
-// issuers on each scheduler
-constexpr int kTcPerRow = 2;
+// softmax threads per query row: one (128 keys, four softmax warps, no row
+// exchange) measured 4 % faster than two (64 keys each, eight warps, maxima
+// and sums exchanged through shared memory), which was 3 % faster than four:
+// fewer ALU-ready warps beside the MMA issuers on each scheduler
+constexpr int kTcPerRow = 1;
 constexpr int kTcRowKeys = 128 / kTcPerRow;   // keys (and output dims) of one thread
 constexpr int kTcChunks = kTcRowKeys / 32;    // 32-column tensor-memory accesses of a thread
 constexpr int kTcRowVec = kTcRowKeys / 8;     // 16-byte pieces of a thread's Q / V row slice
-static_assert(kTcPerRow == 2 || kTcPerRow == 4, "two or four softmax threads per row");
+static_assert(kTcPerRow == 1 || kTcPerRow == 2 || kTcPerRow == 4, "1, 2 or 4 softmax threads per row");
 constexpr int kTcSoftmaxWarps = 4 * kTcPerRow;
 
 constexpr int kTcVWarp = 2 + kTcSoftmaxWarps;  // the V producer, after the softmax warps
@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (warp == 1) tmem_alloc(&tmem_base, kTcCols);
     // Q row r = (token r / G, head r % G), rows past the chunk zero: each of
-    // the row's softmax threads fetches its slice (dims kTcRowKeys part ..)
+    // the row's softmax threads fetches its slice (dims kTcRowKeys part ..;
+    // with one thread per row, the whole row)
     uint32_t qw[kTcRowKeys / 2];
     if (warp >= 2 && warp < kTcVWarp) {
         const int r = (warp & 3) * 32 + lane, part = (warp - 2) >> 2;
@@ -221,10 +222,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0 || warp == kTcVWarp) {
         // ------------------------------------------------------------------
         // producers: K tiles (warp 0, free once S is computed, three stages)
-        // and V tiles (warp 10, held until P V is done, two stages)
+        // and V tiles (warp 6, held until P V is done, two stages)
         // ------------------------------------------------------------------
         if (lane == 0) prefetch_tensor_map(warp == 0 ? &tmap_k : &tmap_v);
-        // warp 0 streams K, warp 10 V, each at its own pace (issuing the
+        // warp 0 streams K, warp 6 V, each at its own pace (issuing the
         // first K tiles before the CTA barrier measured 7 % slower: their
         // block-table reads hold the barrier up)
         bool ok = true;
@@ -290,7 +291,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------------
         // softmax and epilogue: this thread owns slice `part` (kTcRowKeys keys
         // of each tile, kTcRowKeys output dims) of row r (tensor-memory lane
-        // r); the row's threads exchange maxima and sums through shared memory
+        // r); with more than one thread per row they exchange maxima and sums
+        // through shared memory
         // ------------------------------------------------------------------
         const int r = (warp & 3) * 32 + lane, part = (warp - 2) >> 2;
         const int t = r / G, h = r % G;
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         // the row's threads' values, through shared set `set`
         auto exchange = [&](int set, float v) {
+            if (kTcPerRow == 1) return make_float4(v, 0.f, 0.f, 0.f);
             xchg[set][part][r] = v;
             // the row's threads sit in the softmax warps of lane quarter
             // warp % 4: one named barrier (1 + warp % 4) per quarter
@@ -363,8 +366,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // two column sets by tile parity: a set is rewritten only after
                 // every thread has passed the next tile's barrier
                 const float4 e4 = exchange(bb, mx);
-                mx = (kTcPerRow == 2 ? fmaxf(e4.x, e4.y)
-                                     : fmaxf(fmaxf(e4.x, e4.y), fmaxf(e4.z, e4.w))) * sl;   // log2 units
+                mx = (kTcPerRow == 1   ? e4.x
+                      : kTcPerRow == 2 ? fmaxf(e4.x, e4.y)
+                                       : fmaxf(fmaxf(e4.x, e4.y), fmaxf(e4.z, e4.w))) * sl;   // log2 units
             }
             // the reference max: raised only when the row max grows past 2^8
             const bool need = j > 0 && mx > m + kRescaleThresholdLog2;
@@ -456,7 +460,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after_sync();
         const float4 l4 = exchange(2, l);
         if (!failed) {
-            const float inv = 1.f / (kTcPerRow == 2 ? l4.x + l4.y : (l4.x + l4.y) + (l4.z + l4.w));
+            const float inv = 1.f / (kTcPerRow == 1   ? l4.x
+                                     : kTcPerRow == 2 ? l4.x + l4.y
+                                                      : (l4.x + l4.y) + (l4.z + l4.w));
             T* out = reinterpret_cast<T*>(p.out) +
                      ((size_t)(q0 + t0 + min(t, rows - 1)) * p.num_q_heads + (size_t)g * G + h) * 128 +
                      kTcRowKeys * part;
