@@ -253,7 +253,8 @@ int pa_prefill(const void* q, const void* k_cache, const void* v_cache,
  * pa_prefill_ws: pa_prefill with a workspace in which a one-CTA plan kernel
  * orders the tcgen05 kernel's (sequence, chunk) work items by the number of
  * key tiles they read, longest first, so that the longest start first and
- * the SMs finish together (pa_prefill, without one, takes each sequence's
+ * the SMs finish together (the kernel's persistent CTAs, one per SM, deal
+ * that order out in a snake; pa_prefill, without one, takes each sequence's
  * chunks last-first: later chunks read more keys).  The pages describe
  * prefill cost growing with the square of the prompt length (ta-paperlens
  * page, the quadratic cost of prefill); the ordering itself is this
