@@ -35,6 +35,18 @@ def test_named_workload(dev, name):
     print(name, errs)
 
 
+@pytest.mark.parametrize("name", ["llama8b", "prefix", "llama70b", "long16", "long32"])
+def test_fused_step_at_the_benchmarked_partition(dev, name):
+    """The fused step in the launch configuration the benchmark times: the
+    partition size lib.choose_partition picks from the batch's lengths
+    (1024, 1024, 2048, 4096 and 4096 tokens on a 152-SM part)."""
+    w = pin.build_workload(name)
+    P = lib.choose_partition(w.num_seqs, w.num_kv_heads, int(w.context_lens.max()),
+                             w.block_size, dev, w.context_lens)
+    errs = check_workload(w, dev, modes=("fused",), partition_size=P)
+    print(name, P, errs)
+
+
 # ---------------------------------------------------------------------------
 # ragged edges: lengths around tile, block and partition boundaries
 # ---------------------------------------------------------------------------
