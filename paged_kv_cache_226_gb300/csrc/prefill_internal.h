@@ -21,9 +21,10 @@ struct PrefillParams {
     int max_blocks_per_seq;
     int block_size;
     int64_t num_blocks;
-    // tcgen05 kernel only: the order in which its CTAs take (sequence, chunk)
-    // items, num_seqs * max_chunks entries of b * max_chunks + chunk (-1:
-    // none), longest first; null: later chunks (more keys) first
+    // tcgen05 kernel only: the order in which its persistent CTAs deal out
+    // the (sequence, chunk) items, num_seqs * max_chunks entries of b *
+    // max_chunks + chunk (-1: none), longest first; null: later chunks (more
+    // keys) first
     const int32_t* sched;
     int max_chunks;                // chunk slots per sequence
     int num_seqs;
@@ -36,7 +37,7 @@ cudaError_t launch_prefill(int dtype, int head_dim, const CUtensorMap& tmk,
 // tcgen05 chunked prefill (prefill_tc.cu): head_dim 128, groups of 1, 2, 4, 8,
 // a positive softmax scale.
 bool prefill_tc_supported(int head_dim, int group, float scale);
-// Chunk slots per sequence: query tokens per CTA are 128 / group.
+// Chunk slots per sequence: query tokens per work unit are 128 / group.
 int prefill_tc_chunks(int group, int max_query_len);
 // One CTA: writes the order of the num_seqs * max_chunks items, longest
 // (most key tiles) first, to sched (p.sched is ignored).
